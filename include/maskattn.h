@@ -1,0 +1,130 @@
+/*
+ * maskattn.h -- C ABI of libmaskattn: masked attention forward and backward
+ * (GQA/MHA, BHSD, head dim 128, fp16 or bf16, fp32 accumulation) with a
+ * per-head attention sink, for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operation (restated from the pages this library follows):
+ *   - tilelang-ascend PR #1 "Add GQA Sink Backward BHSD", Summary: online
+ *     softmax with an attention sink and a sliding-window mask; commit notes
+ *     of the 2-kernel design: Phase0 Delta = sum(O*dO), a KV loop of five
+ *     contractions + softmax + dS, Phase5 dSink.  The sink is one logit per
+ *     head that joins only the softmax denominator (it has no value row).
+ *   - cannbot-knowledge PR #174, BlockSparseAttentionGrad runbook, task
+ *     features: a uint8 block mask [B,N,ceil(Sq/bx),ceil(Skv/by)] with bx and
+ *     by chosen independently and not required to divide the sequence
+ *     lengths; optimisations 1-2: the host only checks shapes and carves
+ *     memory, the mask is transposed and compacted into select tables on the
+ *     device; optimisation 3: dK/dV are written back contiguously, without
+ *     atomics; precision notes: p = exp(s - lse), ds = p * (dp - delta), a row
+ *     that sees no key gets zeros.
+ *
+ * With g = Hq / Hkv, query head h reads key/value head floor(h / g).
+ * Visibility of key j to query i (0-based):
+ *   ATTN_MASK_NONE     every j
+ *   ATTN_MASK_CAUSAL   j <= i                        (requires Sq == Skv)
+ *   ATTN_MASK_SLIDING  j <= i and i - j < window     (requires Sq == Skv)
+ *   ATTN_MASK_BLOCK    block_mask[b, h, i / bx, j / by] != 0
+ *
+ * Memory: every tensor argument is a DEVICE pointer owned by the caller,
+ * contiguous, 16-byte aligned.  q, o, dO, dq: [B,Hq,Sq,128]; k, v, dk, dv:
+ * [B,Hkv,Skv,128], all of `dtype`; lse: float32 [B,Hq,Sq] (natural log);
+ * sink, dsink: float32 [Hq]; block_mask: uint8 [B,Hq,ceil(Sq/bx),ceil(Skv/by)].
+ * The library allocates no device memory: scratch comes from the caller's
+ * workspace `ws` (size from attn_workspace_size, 256-byte aligned).
+ * Limits: Sq, Skv <= 2^24 and B * Hq <= 65535.
+ *
+ * Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ * default stream), returns a status at once, and may be enqueued again on the
+ * same stream with the same workspace.  Calls that share a workspace must not
+ * overlap in time (use one stream, or one workspace per stream).
+ *
+ * Errors: arguments are checked on the host before anything is enqueued; on
+ * an error nothing is enqueued and the outputs are left untouched.  Device
+ * waits inside the kernels are bounded: a wait that runs out records
+ * ATTN_ERR_TIMEOUT in the workspace status word, which attn_get_device_status
+ * reads back.
+ */
+#ifndef MASKATTN_H_
+#define MASKATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* bad shape, null or misaligned pointer, bad mask fields */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (D != 128) */
+  ATTN_ERR_WORKSPACE = 3,   /* ws_bytes smaller than attn_workspace_size() */
+  ATTN_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  ATTN_ERR_TIMEOUT = 5      /* a device-side wait ran out (read back by attn_get_device_status) */
+} attn_status_t;
+
+typedef enum { ATTN_F16 = 0, ATTN_BF16 = 1 } attn_dtype_t;
+
+typedef enum {
+  ATTN_MASK_NONE = 0,
+  ATTN_MASK_CAUSAL = 1,
+  ATTN_MASK_SLIDING = 2, /* causal with a window of `window` keys including the diagonal */
+  ATTN_MASK_BLOCK = 3
+} attn_mask_kind_t;
+
+/* Shapes of one call; tensors are contiguous BHSD. */
+typedef struct {
+  int B, Hq, Hkv, Sq, Skv, D;
+  int dtype; /* attn_dtype_t */
+} attn_shape_t;
+
+/* Mask description.  window is read for ATTN_MASK_SLIDING only; bx, by and
+ * block_mask for ATTN_MASK_BLOCK only (block_mask is a device pointer). */
+typedef struct {
+  int kind; /* attn_mask_kind_t */
+  int window;
+  int bx, by;
+  const uint8_t* block_mask;
+} attn_mask_desc_t;
+
+/* Workspace bytes needed by attn_fwd and attn_bwd for this shape and mask.
+ * Host only; never touches the GPU.  Errors: ATTN_ERR_INVALID_ARG,
+ * ATTN_ERR_UNSUPPORTED (same checks as attn_bwd, pointers not required). */
+attn_status_t attn_workspace_size(const attn_shape_t* shape, const attn_mask_desc_t* mask,
+                                  size_t* bytes);
+
+/* Forward: O = softmax_with_sink(scale * q k^T, masked) v, and
+ * lse[b,h,i] = log(sum_j exp(scale*s_ij) + exp(sink_h)) over visible j.
+ * sink may be NULL (no sink).  A row with no visible key and no sink gets
+ * O = 0 and lse = +inf.  Outputs: o (dtype), lse (float32). */
+attn_status_t attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void* v,
+                       const float* sink, const attn_mask_desc_t* mask, float scale, void* o,
+                       float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward from the forward's o and lse (taken as given):
+ *   Delta_i = sum_d dO_id o_id;  P_ij = exp(scale*s_ij - lse_i);
+ *   dS_ij = P_ij (dO_i . v_j - Delta_i);
+ *   dq_i = scale sum_j dS_ij k_j;  dk_j = scale sum_{h in group} sum_i dS_ij q_i;
+ *   dv_j = sum_{h in group} sum_i P_ij dO_i;
+ *   dsink_h = - sum_b sum_i exp(sink_h - lse_i) Delta_i.
+ * sink NULL means no sink; dsink is then not written and may be NULL.
+ * Every element of dq, dk, dv (and dsink) is written.  Outputs dq, dk, dv
+ * have `dtype` (fp32 accumulation, round to nearest even). */
+attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, const void* v,
+                       const void* o, const void* dO, const float* lse, const float* sink,
+                       const attn_mask_desc_t* mask, float scale, void* dq, void* dk, void* dv,
+                       float* dsink, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronizes `stream`, then reads the status word that the last call which
+ * used `ws` left in the workspace: ATTN_OK, or ATTN_ERR_TIMEOUT when a device
+ * wait ran out.  ATTN_ERR_CUDA if the synchronization itself fails. */
+attn_status_t attn_get_device_status(const void* ws, void* stream);
+
+/* Static string naming a status code ("ATTN_OK", ...). Never NULL. */
+const char* attn_status_string(attn_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MASKATTN_H_ */

@@ -1,0 +1,189 @@
+"""ctypes binding of libmaskattn (include/maskattn.h), same names as the C ABI.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  PyTorch supplies device memory and the current stream.  If the
+library cannot be built or loaded, every call raises -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, \
+    ATTN_ERR_TIMEOUT = range(6)
+ATTN_F16, ATTN_BF16 = 0, 1
+ATTN_MASK_NONE, ATTN_MASK_CAUSAL, ATTN_MASK_SLIDING, ATTN_MASK_BLOCK = range(4)
+
+# Every symbol include/maskattn.h declares.
+EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_get_device_status",
+           "attn_status_string")
+
+
+class attn_shape_t(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+                ("Sq", ctypes.c_int), ("Skv", ctypes.c_int), ("D", ctypes.c_int),
+                ("dtype", ctypes.c_int)]
+
+
+class attn_mask_desc_t(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("window", ctypes.c_int), ("bx", ctypes.c_int),
+                ("by", ctypes.c_int), ("block_mask", ctypes.c_void_p)]
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {attn_status_string(code)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(build: bool = True) -> ctypes.CDLL:
+    """Load libmaskattn.so (building it first when sources are newer)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build else _build.LIB
+            lib = ctypes.CDLL(path)
+            vp, sz = ctypes.c_void_p, ctypes.c_size_t
+            ps, pm = ctypes.POINTER(attn_shape_t), ctypes.POINTER(attn_mask_desc_t)
+            lib.attn_workspace_size.argtypes = [ps, pm, ctypes.POINTER(sz)]
+            lib.attn_workspace_size.restype = ctypes.c_int
+            lib.attn_fwd.argtypes = [ps, vp, vp, vp, vp, pm, ctypes.c_float, vp, vp, vp, sz, vp]
+            lib.attn_fwd.restype = ctypes.c_int
+            lib.attn_bwd.argtypes = [ps, vp, vp, vp, vp, vp, vp, vp, pm, ctypes.c_float,
+                                     vp, vp, vp, vp, vp, sz, vp]
+            lib.attn_bwd.restype = ctypes.c_int
+            lib.attn_get_device_status.argtypes = [vp, vp]
+            lib.attn_get_device_status.restype = ctypes.c_int
+            lib.attn_status_string.argtypes = [ctypes.c_int]
+            lib.attn_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+# ------------------------------------------------------------------ raw C ABI
+
+def attn_status_string(code: int) -> str:
+    return load().attn_status_string(int(code)).decode()
+
+
+def attn_workspace_size(shape: attn_shape_t, mask: attn_mask_desc_t):
+    n = ctypes.c_size_t(0)
+    r = load().attn_workspace_size(ctypes.byref(shape), ctypes.byref(mask), ctypes.byref(n))
+    return r, n.value
+
+
+def attn_fwd(shape, q, k, v, sink, mask, scale, o, lse, ws, ws_bytes, stream) -> int:
+    return load().attn_fwd(ctypes.byref(shape), q, k, v, sink, ctypes.byref(mask),
+                           ctypes.c_float(scale), o, lse, ws, ws_bytes, stream)
+
+
+def attn_bwd(shape, q, k, v, o, dO, lse, sink, mask, scale, dq, dk, dv, dsink, ws, ws_bytes,
+             stream) -> int:
+    return load().attn_bwd(ctypes.byref(shape), q, k, v, o, dO, lse, sink, ctypes.byref(mask),
+                           ctypes.c_float(scale), dq, dk, dv, dsink, ws, ws_bytes, stream)
+
+
+def attn_get_device_status(ws, stream) -> int:
+    return load().attn_get_device_status(ws, stream)
+
+
+# ------------------------------------------------------------- torch helpers
+
+@dataclass
+class Mask:
+    kind: int = ATTN_MASK_NONE
+    window: int = 0
+    bx: int = 1
+    by: int = 1
+    block_mask: Optional[torch.Tensor] = None   # uint8 [B,Hq,nQB,nKB] on the device
+
+    def desc(self) -> attn_mask_desc_t:
+        bm = self.block_mask.data_ptr() if self.block_mask is not None else None
+        return attn_mask_desc_t(self.kind, self.window, self.bx, self.by, bm)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return ATTN_F16
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def shape_of(q: torch.Tensor, k: torch.Tensor) -> attn_shape_t:
+    B, Hq, Sq, D = q.shape
+    _, Hkv, Skv, _ = k.shape
+    return attn_shape_t(B, Hq, Hkv, Sq, Skv, D, _dtype_code(q))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace(shape: attn_shape_t, mask: Mask, device) -> torch.Tensor:
+    r, n = attn_workspace_size(shape, mask.desc())
+    if r != ATTN_OK:
+        raise AttnError(r, "attn_workspace_size")
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def _check(t: torch.Tensor, name: str):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def fwd(q, k, v, sink, mask: Mask, scale: float, ws: Optional[torch.Tensor] = None,
+        stream=None):
+    """Forward; returns (o, lse)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    shape = shape_of(q, k)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(shape, mask, q.device)
+    r = attn_fwd(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(sink), mask.desc(), scale, _ptr(o),
+                 _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    if r != ATTN_OK:
+        raise AttnError(r, "attn_fwd")
+    return o, lse
+
+
+def bwd(q, k, v, o, dO, lse, sink, mask: Mask, scale: float, ws: Optional[torch.Tensor] = None,
+        out=None, stream=None):
+    """Backward; returns (dq, dk, dv, dsink) (dsink is None without a sink)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (lse, "lse")):
+        _check(t, n)
+    shape = shape_of(q, k)
+    if out is None:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dsink = torch.empty_like(sink) if sink is not None else None
+    else:
+        dq, dk, dv, dsink = out
+    if ws is None:
+        ws = workspace(shape, mask, q.device)
+    r = attn_bwd(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(sink),
+                 mask.desc(), scale, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dsink), _ptr(ws),
+                 ws.numel(), _stream(stream))
+    if r != ATTN_OK:
+        raise AttnError(r, "attn_bwd")
+    return dq, dk, dv, dsink
+
+
+def device_status(ws: torch.Tensor, stream=None) -> int:
+    return attn_get_device_status(_ptr(ws), _stream(stream))

@@ -1,0 +1,284 @@
+// api.cu -- the C ABI of libmaskattn (declared in include/maskattn.h).
+//
+// The host side only checks arguments, carves the caller's workspace and
+// enqueues kernels on the caller's stream: no dense token mask is built and
+// nothing is allocated (cannbot-knowledge PR #174, BlockSparseAttentionGrad
+// runbook, optimisation 1: the host does shape, alloc and view only).
+//
+// attn_bwd enqueues, in order:
+//   k_preprocess        Delta, lse*log2(e) (padded), dSink partials
+//   k_mask_transpose +  block masks only: transposed mask and both
+//   k_build_sel           select tables
+//   k_dkdv              key-stationary dK / dV
+//   k_qside<dQ>         query-stationary dQ
+//   k_dsink_finalize    sink only: dSink = -sum of partials
+#include <stdlib.h>
+#include <string.h>
+
+#include "../../include/maskattn.h"
+#include "internal.h"
+#include "tmap.h"
+
+using namespace mab;
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+attn_status_t check_shape_mask(const attn_shape_t* sh, const attn_mask_desc_t* mk) {
+  if (!sh || !mk) return ATTN_ERR_INVALID_ARG;
+  if (sh->B <= 0 || sh->Hq <= 0 || sh->Hkv <= 0 || sh->Sq <= 0 || sh->Skv <= 0 || sh->D <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (sh->Hq % sh->Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (sh->dtype != ATTN_F16 && sh->dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  // sequence lengths up to 2^24 and B*Hq up to 65535 keep every index and
+  // grid dimension in range
+  if (sh->Sq > (1 << 24) || sh->Skv > (1 << 24) || (long long)sh->B * sh->Hq > 65535)
+    return ATTN_ERR_INVALID_ARG;
+  switch (mk->kind) {
+    case ATTN_MASK_NONE:
+      break;
+    case ATTN_MASK_CAUSAL:
+      if (sh->Sq != sh->Skv) return ATTN_ERR_INVALID_ARG;
+      break;
+    case ATTN_MASK_SLIDING:
+      if (sh->Sq != sh->Skv || mk->window < 1) return ATTN_ERR_INVALID_ARG;
+      break;
+    case ATTN_MASK_BLOCK:
+      if (mk->bx < 1 || mk->by < 1) return ATTN_ERR_INVALID_ARG;
+      break;
+    default:
+      return ATTN_ERR_INVALID_ARG;
+  }
+  if (sh->D != HEAD_DIM) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+struct Dims {
+  int Sq_pad, nqb, nkb, nQT_k, nKT_k, nQT_q, nKT_q, nparts;
+};
+
+Dims dims_of(const attn_shape_t* sh, const attn_mask_desc_t* mk) {
+  Dims d;
+  d.Sq_pad = (sh->Sq + PREP_ROWS - 1) / PREP_ROWS * PREP_ROWS;
+  const bool blk = mk->kind == ATTN_MASK_BLOCK;
+  d.nqb = blk ? (sh->Sq + mk->bx - 1) / mk->bx : 0;
+  d.nkb = blk ? (sh->Skv + mk->by - 1) / mk->by : 0;
+  d.nQT_k = (sh->Sq + KV_SUB - 1) / KV_SUB;
+  d.nKT_k = (sh->Skv + KV_TILE - 1) / KV_TILE;
+  d.nQT_q = (sh->Sq + Q_TILE - 1) / Q_TILE;
+  d.nKT_q = (sh->Skv + Q_SUB - 1) / Q_SUB;
+  d.nparts = sh->B * (d.Sq_pad / PREP_ROWS);
+  return d;
+}
+
+WsLayout layout_of(const attn_shape_t* sh, const attn_mask_desc_t* mk) {
+  Dims d = dims_of(sh, mk);
+  const size_t BH = (size_t)sh->B * sh->Hq;
+  WsLayout L;
+  size_t off = 0;
+  L.status = off;
+  off = align256(off + sizeof(DevStatus));
+  L.lse2 = off;
+  off = align256(off + BH * d.Sq_pad * sizeof(float));
+  L.delta = off;
+  off = align256(off + BH * d.Sq_pad * sizeof(float));
+  L.dsink_part = off;
+  off = align256(off + (size_t)sh->Hq * d.nparts * sizeof(float));
+  L.maskT = L.sel_k = L.cnt_k = L.sel_q = L.cnt_q = off;
+  if (mk->kind == ATTN_MASK_BLOCK) {
+    L.maskT = off;
+    off = align256(off + BH * d.nqb * d.nkb);
+    L.sel_k = off;
+    off = align256(off + BH * d.nKT_k * d.nQT_k * sizeof(int));
+    L.cnt_k = off;
+    off = align256(off + BH * d.nKT_k * sizeof(int));
+    L.sel_q = off;
+    off = align256(off + BH * d.nQT_q * d.nKT_q * sizeof(int));
+    L.cnt_q = off;
+    off = align256(off + BH * d.nQT_q * sizeof(int));
+  }
+  L.total = off;
+  return L;
+}
+
+unsigned long long wait_timeout_ns() {
+  const char* e = getenv("MASKATTN_WAIT_TIMEOUT_NS");
+  if (e && *e) {
+    unsigned long long v = strtoull(e, nullptr, 10);
+    if (v > 0) return v;
+  }
+  return kDefaultTimeoutNs;
+}
+
+AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const WsLayout& L,
+                     uint8_t* ws, float scale) {
+  Dims d = dims_of(sh, mk);
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  p.B = sh->B;
+  p.Hq = sh->Hq;
+  p.Hkv = sh->Hkv;
+  p.Sq = sh->Sq;
+  p.Skv = sh->Skv;
+  p.group = sh->Hq / sh->Hkv;
+  p.Sq_pad = d.Sq_pad;
+  p.mask_kind = mk->kind;
+  p.window = mk->kind == ATTN_MASK_SLIDING ? mk->window : 0;
+  p.bx = mk->kind == ATTN_MASK_BLOCK ? mk->bx : 1;
+  p.by = mk->kind == ATTN_MASK_BLOCK ? mk->by : 1;
+  p.nqb = d.nqb;
+  p.nkb = d.nkb;
+  if (mk->kind == ATTN_MASK_BLOCK) {
+    p.mask = mk->block_mask;
+    p.maskT = ws + L.maskT;
+    p.sel_k = reinterpret_cast<const int*>(ws + L.sel_k);
+    p.cnt_k = reinterpret_cast<const int*>(ws + L.cnt_k);
+    p.sel_q = reinterpret_cast<const int*>(ws + L.sel_q);
+    p.cnt_q = reinterpret_cast<const int*>(ws + L.cnt_q);
+  }
+  p.nQT_k = d.nQT_k;
+  p.nKT_k = d.nKT_k;
+  p.nQT_q = d.nQT_q;
+  p.nKT_q = d.nKT_q;
+  p.lse2 = reinterpret_cast<const float*>(ws + L.lse2);
+  p.delta = reinterpret_cast<const float*>(ws + L.delta);
+  p.scale = scale;
+  p.scale_log2 = scale * LOG2E;
+  p.status = reinterpret_cast<DevStatus*>(ws + L.status);
+  p.timeout_ns = wait_timeout_ns();
+  return p;
+}
+
+attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// Transposed mask and both select tables (block masks only).
+cudaError_t enqueue_tables(const attn_shape_t* sh, const WsLayout& L, uint8_t* ws,
+                           const AttnParams& p, cudaStream_t st) {
+  cudaError_t e = launch_mask_transpose(p.mask, ws + L.maskT, sh->B * sh->Hq, p.nqb, p.nkb, st);
+  if (e != cudaSuccess) return e;
+  return launch_build_sel(p, reinterpret_cast<int*>(ws + L.sel_k),
+                          reinterpret_cast<int*>(ws + L.cnt_k),
+                          reinterpret_cast<int*>(ws + L.sel_q),
+                          reinterpret_cast<int*>(ws + L.cnt_q), st);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+attn_status_t attn_workspace_size(const attn_shape_t* shape, const attn_mask_desc_t* mask,
+                                  size_t* bytes) {
+  if (!bytes) return ATTN_ERR_INVALID_ARG;
+  attn_status_t r = check_shape_mask(shape, mask);
+  if (r != ATTN_OK) return r;
+  *bytes = layout_of(shape, mask).total;
+  return ATTN_OK;
+}
+
+attn_status_t attn_fwd(const attn_shape_t* shape, const void* q, const void* k, const void* v,
+                       const float* sink, const attn_mask_desc_t* mask, float scale, void* o,
+                       float* lse, void* ws, size_t ws_bytes, void* stream) {
+  attn_status_t r = check_shape_mask(shape, mask);
+  if (r != ATTN_OK) return r;
+  if (!q || !k || !v || !o || !lse || !ws) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4) || !aligned(ws, 256) || (sink && !aligned(sink, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  if (mask->kind == ATTN_MASK_BLOCK && !mask->block_mask) return ATTN_ERR_INVALID_ARG;
+  const WsLayout L = layout_of(shape, mask);
+  if (ws_bytes < L.total) return ATTN_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const bool bf16 = shape->dtype == ATTN_BF16;
+  AttnParams p = params_of(shape, mask, L, w, scale);
+  p.sink = sink;
+  p.lse_out = lse;
+  const int BH = shape->B * shape->Hq, BHkv = shape->B * shape->Hkv;
+  CUtensorMap tQ, tK, tV;
+  if (!make_bhsd_map(&tQ, q, bf16, BH, shape->Sq, Q_TILE) ||
+      !make_bhsd_map(&tK, k, bf16, BHkv, shape->Skv, Q_SUB) ||
+      !make_bhsd_map(&tV, v, bf16, BHkv, shape->Skv, Q_SUB))
+    return ATTN_ERR_CUDA;
+  cudaError_t e = cudaMemsetAsync(w + L.status, 0, sizeof(DevStatus), st);
+  if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) e = enqueue_tables(shape, L, w, p, st);
+  if (e == cudaSuccess) e = launch_fwd(bf16, p, tQ, tK, tV, o, st);
+  return cuda_status(e);
+}
+
+attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, const void* v,
+                       const void* o, const void* dO, const float* lse, const float* sink,
+                       const attn_mask_desc_t* mask, float scale, void* dq, void* dk, void* dv,
+                       float* dsink, void* ws, size_t ws_bytes, void* stream) {
+  attn_status_t r = check_shape_mask(shape, mask);
+  if (r != ATTN_OK) return r;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv || !ws || (sink && !dsink))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(dO, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(ws, 256) || (sink && (!aligned(sink, 4) || !aligned(dsink, 4))))
+    return ATTN_ERR_INVALID_ARG;
+  if (mask->kind == ATTN_MASK_BLOCK && !mask->block_mask) return ATTN_ERR_INVALID_ARG;
+  const WsLayout L = layout_of(shape, mask);
+  if (ws_bytes < L.total) return ATTN_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const bool bf16 = shape->dtype == ATTN_BF16;
+  AttnParams p = params_of(shape, mask, L, w, scale);
+  const Dims d = dims_of(shape, mask);
+  const int BH = shape->B * shape->Hq, BHkv = shape->B * shape->Hkv;
+
+  // dK/dV walk query sub-tiles of KV_SUB rows over key tiles of KV_TILE rows;
+  // dQ walks key sub-tiles of Q_SUB rows over query tiles of Q_TILE rows.
+  CUtensorMap tQs, tdOs, tKt, tVt, tQt, tdOt, tKs, tVs;
+  if (!make_bhsd_map(&tQs, q, bf16, BH, shape->Sq, KV_SUB) ||
+      !make_bhsd_map(&tdOs, dO, bf16, BH, shape->Sq, KV_SUB) ||
+      !make_bhsd_map(&tKt, k, bf16, BHkv, shape->Skv, KV_TILE) ||
+      !make_bhsd_map(&tVt, v, bf16, BHkv, shape->Skv, KV_TILE) ||
+      !make_bhsd_map(&tQt, q, bf16, BH, shape->Sq, Q_TILE) ||
+      !make_bhsd_map(&tdOt, dO, bf16, BH, shape->Sq, Q_TILE) ||
+      !make_bhsd_map(&tKs, k, bf16, BHkv, shape->Skv, Q_SUB) ||
+      !make_bhsd_map(&tVs, v, bf16, BHkv, shape->Skv, Q_SUB))
+    return ATTN_ERR_CUDA;
+
+  cudaError_t e = cudaMemsetAsync(w + L.status, 0, sizeof(DevStatus), st);
+  if (e == cudaSuccess)
+    e = launch_preprocess(bf16, o, dO, lse, sink, reinterpret_cast<float*>(w + L.lse2),
+                          reinterpret_cast<float*>(w + L.delta),
+                          reinterpret_cast<float*>(w + L.dsink_part), shape->B, shape->Hq,
+                          shape->Sq, d.Sq_pad, st);
+  if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) e = enqueue_tables(shape, L, w, p, st);
+  if (e == cudaSuccess) e = launch_dkdv(bf16, p, tQs, tdOs, tKt, tVt, dk, dv, st);
+  if (e == cudaSuccess) e = launch_dq(bf16, p, tQt, tdOt, tKs, tVs, dq, st);
+  if (e == cudaSuccess && sink)
+    e = launch_dsink_finalize(reinterpret_cast<const float*>(w + L.dsink_part), shape->Hq,
+                              d.nparts, dsink, st);
+  return cuda_status(e);
+}
+
+attn_status_t attn_get_device_status(const void* ws, void* stream) {
+  if (!ws) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return ATTN_ERR_CUDA;
+  DevStatus h;
+  if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  return h.code == 0 ? ATTN_OK : static_cast<attn_status_t>(h.code);
+}
+
+}  // extern "C"

@@ -1,0 +1,171 @@
+// tiles.cuh -- device helpers shared by the contraction kernels: per-thread
+// visibility bitmasks for 32 consecutive partner positions, the walk over
+// active partner tiles (closed form for causal / sliding / none, select tables
+// for block masks), and a coalesced per-warp row store.
+#pragma once
+#include "internal.h"
+
+namespace mab {
+
+// Bits [lo, hi] (inclusive, clipped to [0, 31]) set.
+__device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
+  if (lo < 0) lo = 0;
+  if (hi > 31) hi = 31;
+  if (hi < lo) return 0u;
+  uint32_t upper = (hi == 31) ? 0xffffffffu : ((1u << (hi + 1)) - 1u);
+  return upper & ~((1u << lo) - 1u);
+}
+
+// Query row i against keys j0 .. j0+31 (bit c <-> key j0 + c).
+__device__ __forceinline__ uint32_t vis_query_row(const AttnParams& p, int bh, int i, int j0) {
+  if (i >= p.Sq) return 0u;
+  uint32_t inrange = bit_range(0, p.Skv - 1 - j0);
+  switch (p.mask_kind) {
+    case MK_NONE:
+      return inrange;
+    case MK_CAUSAL:
+      return inrange & bit_range(0, i - j0);
+    case MK_SLIDING:
+      return inrange & bit_range(i - p.window + 1 - j0, i - j0);
+    default: {
+      const uint8_t* row = p.mask + ((size_t)bh * p.nqb + i / p.bx) * p.nkb;
+      int jend = min(j0 + 31, p.Skv - 1);
+      if (jend < j0) return 0u;
+      uint32_t m = 0;
+      for (int kb = j0 / p.by; kb * p.by <= jend; ++kb)
+        if (row[kb]) m |= bit_range(kb * p.by - j0, (kb + 1) * p.by - 1 - j0);
+      return m & inrange;
+    }
+  }
+}
+
+// Key row j against queries i0 .. i0+31 (bit c <-> query i0 + c).
+__device__ __forceinline__ uint32_t vis_key_row(const AttnParams& p, int bh, int j, int i0) {
+  if (j >= p.Skv) return 0u;
+  uint32_t inrange = bit_range(0, p.Sq - 1 - i0);
+  switch (p.mask_kind) {
+    case MK_NONE:
+      return inrange;
+    case MK_CAUSAL:
+      return inrange & bit_range(j - i0, 31);
+    case MK_SLIDING:
+      return inrange & bit_range(j - i0, j + p.window - 1 - i0);
+    default: {
+      const uint8_t* row = p.maskT + ((size_t)bh * p.nkb + j / p.by) * p.nqb;
+      int iend = min(i0 + 31, p.Sq - 1);
+      if (iend < i0) return 0u;
+      uint32_t m = 0;
+      for (int qb = i0 / p.bx; qb * p.bx <= iend; ++qb)
+        if (row[qb]) m |= bit_range(qb * p.bx - i0, (qb + 1) * p.bx - 1 - i0);
+      return m & inrange;
+    }
+  }
+}
+
+// Walk of a query-tile CTA (Q_TILE rows of head bh) over key sub-tiles of
+// Q_SUB rows.
+struct QWalk {
+  int lo, cnt;
+  const int* list;  // select-table row, or nullptr for the closed form
+  __device__ __forceinline__ void init(const AttnParams& p, int bh, int qt) {
+    if (p.mask_kind == MK_BLOCK) {
+      size_t row = (size_t)bh * p.nQT_q + qt;
+      list = p.sel_q + row * p.nKT_q;
+      cnt = p.cnt_q[row];
+      lo = 0;
+    } else {
+      int hi;
+      int q0 = qt * Q_TILE;
+      partner_range(p.mask_kind, p.window, true, q0, min(q0 + Q_TILE, p.Sq), Q_SUB, p.Skv, &lo,
+                    &hi);
+      cnt = hi - lo + 1;
+      if (cnt < 0) cnt = 0;
+      list = nullptr;
+    }
+  }
+  __device__ __forceinline__ int tile(int n) const { return list ? list[n] : lo + n; }
+};
+
+// Walk of a key-tile CTA (KV_TILE rows of kv head (b, c)) over (query head of
+// the group, query sub-tile of KV_SUB rows) pairs, head-major.
+struct KVWalk {
+  int lo, cnt_closed;
+  int b, c, t;
+  __device__ __forceinline__ void init(const AttnParams& p, int b_, int c_, int t_) {
+    b = b_;
+    c = c_;
+    t = t_;
+    lo = 0;
+    cnt_closed = 0;
+    if (p.mask_kind != MK_BLOCK) {
+      int hi;
+      int k0 = t * KV_TILE;
+      partner_range(p.mask_kind, p.window, false, k0, min(k0 + KV_TILE, p.Skv), KV_SUB, p.Sq, &lo,
+                    &hi);
+      cnt_closed = hi - lo + 1;
+      if (cnt_closed < 0) cnt_closed = 0;
+    }
+  }
+  __device__ __forceinline__ int count(const AttnParams& p, int hh) const {
+    if (p.mask_kind != MK_BLOCK) return cnt_closed;
+    int bh = b * p.Hq + c * p.group + hh;
+    return p.cnt_k[(size_t)bh * p.nKT_k + t];
+  }
+  __device__ __forceinline__ int tile(const AttnParams& p, int hh, int idx) const {
+    if (p.mask_kind != MK_BLOCK) return lo + idx;
+    int bh = b * p.Hq + c * p.group + hh;
+    return p.sel_k[((size_t)bh * p.nKT_k + t) * p.nQT_k + idx];
+  }
+  __device__ __forceinline__ int total(const AttnParams& p) const {
+    if (p.mask_kind != MK_BLOCK) return cnt_closed * p.group;
+    int s = 0;
+    for (int hh = 0; hh < p.group; ++hh) s += count(p, hh);
+    return s;
+  }
+};
+
+// Sequential cursor over a KVWalk: yields (hh, idx) in walk order.
+struct KVCursor {
+  int hh, idx, cnt;
+  __device__ __forceinline__ void start(const AttnParams& p, const KVWalk& w) {
+    hh = 0;
+    idx = 0;
+    cnt = w.count(p, 0);
+    skip(p, w);
+  }
+  __device__ __forceinline__ void skip(const AttnParams& p, const KVWalk& w) {
+    while (idx >= cnt && hh < p.group) {
+      ++hh;
+      idx = 0;
+      cnt = hh < p.group ? w.count(p, hh) : 0;
+    }
+  }
+  __device__ __forceinline__ void next(const AttnParams& p, const KVWalk& w) {
+    ++idx;
+    skip(p, w);
+  }
+};
+
+// Store 32 rows x 64 columns (16-bit elements, packed as 32 u32 per lane, one
+// row per lane) through a per-warp 4 KB staging buffer so that global stores
+// are 128-byte coalesced.  out_row0 points at column col0 of the warp's first
+// row; row stride is HEAD_DIM elements; rows >= nvalid are skipped.
+__device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint32_t (&pk)[32],
+                                                uint16_t* out_row0, int nvalid) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    int row = k * 4 + (lane >> 3), c = lane & 7;
+    uint4 v = *reinterpret_cast<const uint4*>(stage + row * 128 + ((c ^ (row & 7)) << 4));
+    if (row < nvalid) *reinterpret_cast<uint4*>(out_row0 + (size_t)row * HEAD_DIM + c * 8) = v;
+  }
+  __syncwarp();
+}
+
+}  // namespace mab

@@ -1,0 +1,141 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path and the oracle on
+the same seeded inputs and compare them under the acceptance gate.
+
+Gate (per output tensor): no non-finite element, and
+|gpu - ref| <= atol + rtol * |ref| on at least 99.9 % of the elements, with
+atol = rtol = 2e-3 for fp16 inputs and 1.6e-2 for bf16 inputs.  The oracle
+reference is float64 computed from the very values the GPU received (inputs
+rounded to the working dtype, O rounded to the dtype, LSE rounded to fp32).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+import oracle
+from masked_attention_backward_gb300 import binding as mab
+from masked_attention_backward_gb300.workloads import MASK_BLOCK, Inputs, Workload, make_inputs
+
+TOL = {"f16": 2e-3, "bf16": 1.6e-2}
+MIN_FRAC = 0.999
+
+
+def oracle_problem(wl: Workload, inp: Inputs) -> oracle.Problem:
+    return oracle.Problem(
+        B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, Sq=wl.Sq, Skv=wl.Skv, D=wl.D, scale=wl.scale,
+        mask_kind=wl.mask_kind, window=wl.window, bx=wl.bx, by=wl.by,
+        block_mask=None if inp.block_mask is None else inp.block_mask.numpy(),
+        sink=None if inp.sink is None else inp.sink.double().numpy())
+
+
+def gpu_mask(wl: Workload, inp: Inputs, device="cuda") -> mab.Mask:
+    bm = inp.block_mask.to(device) if inp.block_mask is not None else None
+    return mab.Mask(kind=wl.mask_kind, window=wl.window, bx=wl.bx, by=wl.by, block_mask=bm)
+
+
+def forward_stats(wl: Workload, inp: Inputs, pb=None):
+    """Oracle forward; returns (O rounded to the dtype, LSE rounded to fp32)."""
+    pb = pb or oracle_problem(wl, inp)
+    O, lse = oracle.forward(pb, inp.q, inp.k, inp.v)
+    return torch.from_numpy(O).to(wl.torch_dtype), torch.from_numpy(lse).to(torch.float32)
+
+
+def compare(name: str, got, ref, dtype: str, min_frac: float = MIN_FRAC):
+    """Assert the gate; returns a small report dict."""
+    g = got.detach().to("cpu").double().numpy() if hasattr(got, "detach") else np.asarray(got)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, (name, g.shape, r.shape)
+    nonfinite = int(np.size(g) - np.isfinite(g).sum())
+    assert nonfinite == 0, f"{name}: {nonfinite} non-finite elements"
+    tol = TOL[dtype]
+    err = np.abs(g - r)
+    ok = err <= tol + tol * np.abs(r)
+    frac = float(ok.mean()) if ok.size else 1.0
+    rep = {"name": name, "frac": frac, "max_err": float(err.max()) if err.size else 0.0,
+           "n": int(ok.size)}
+    assert frac >= min_frac, f"{name}: only {frac:.5f} within tolerance (max err {rep['max_err']:.3g})"
+    return rep
+
+
+@dataclass
+class GpuRun:
+    dq: torch.Tensor
+    dk: torch.Tensor
+    dv: torch.Tensor
+    dsink: torch.Tensor
+    ws: torch.Tensor
+
+
+def run_gpu_bwd(wl: Workload, inp: Inputs, O, lse, poison: bool = True) -> GpuRun:
+    dev = "cuda"
+    q, k, v, dO = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.dO))
+    o, l = O.to(dev), lse.to(dev)
+    sink = inp.sink.to(dev) if inp.sink is not None else None
+    mask = gpu_mask(wl, inp, dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dsink = torch.empty_like(sink) if sink is not None else None
+    if poison:  # every output element must be written
+        for t in (dq, dk, dv):
+            t.fill_(float("nan"))
+        if dsink is not None:
+            dsink.fill_(float("nan"))
+    ws = mab.workspace(mab.shape_of(q, k), mask, dev)
+    mab.bwd(q, k, v, o, dO, l, sink, mask, wl.scale, ws=ws, out=(dq, dk, dv, dsink))
+    torch.cuda.synchronize()
+    st = mab.device_status(ws)
+    assert st == mab.ATTN_OK, mab.attn_status_string(st)
+    return GpuRun(dq, dk, dv, dsink, ws)
+
+
+def full_parity(wl: Workload, seed=None):
+    """Element-by-element parity of dq, dk, dv (and dsink) against the oracle."""
+    inp = make_inputs(wl, seed)
+    pb = oracle_problem(wl, inp)
+    O, lse = forward_stats(wl, inp, pb)
+    run = run_gpu_bwd(wl, inp, O, lse)
+    ref = oracle.backward(pb, inp.q, inp.k, inp.v, O, inp.dO, lse)
+    reps = [compare("dq", run.dq, ref["dq"], wl.dtype),
+            compare("dk", run.dk, ref["dk"], wl.dtype),
+            compare("dv", run.dv, ref["dv"], wl.dtype)]
+    if inp.sink is not None:
+        reps.append(compare("dsink", run.dsink, ref["dsink"], wl.dtype, min_frac=1.0))
+    return reps, run, ref
+
+
+# Tile sizes of the CUDA kernels (key tile / query sub-tile of the dK-dV walk,
+# query tile / key sub-tile of the dQ walk) and the workspace layout that the
+# library carves; mirrored here so that tests can read the device tables.
+KV_TILE, KV_SUB, Q_TILE, Q_SUB, PREP_ROWS = 128, 64, 128, 64, 128
+
+
+def _a256(x):
+    return (x + 255) // 256 * 256
+
+
+def ws_layout(wl: Workload) -> dict:
+    cdiv = lambda a, b: -(-a // b)
+    Sq_pad = cdiv(wl.Sq, PREP_ROWS) * PREP_ROWS
+    BH = wl.B * wl.Hq
+    L = {"status": 0}
+    off = _a256(16)
+    L["lse2"] = off; off = _a256(off + BH * Sq_pad * 4)
+    L["delta"] = off; off = _a256(off + BH * Sq_pad * 4)
+    L["dsink_part"] = off; off = _a256(off + wl.Hq * wl.B * (Sq_pad // PREP_ROWS) * 4)
+    d = {"Sq_pad": Sq_pad, "nQT_k": cdiv(wl.Sq, KV_SUB), "nKT_k": cdiv(wl.Skv, KV_TILE),
+         "nQT_q": cdiv(wl.Sq, Q_TILE), "nKT_q": cdiv(wl.Skv, Q_SUB)}
+    if wl.mask_kind == MASK_BLOCK:
+        L["maskT"] = off; off = _a256(off + BH * wl.nqb * wl.nkb)
+        L["sel_k"] = off; off = _a256(off + BH * d["nKT_k"] * d["nQT_k"] * 4)
+        L["cnt_k"] = off; off = _a256(off + BH * d["nKT_k"] * 4)
+        L["sel_q"] = off; off = _a256(off + BH * d["nQT_q"] * d["nKT_q"] * 4)
+        L["cnt_q"] = off; off = _a256(off + BH * d["nQT_q"] * 4)
+    L["total"] = off
+    L.update(d)
+    return L
+
+
+def ws_view(ws: torch.Tensor, off: int, count: int, dtype) -> torch.Tensor:
+    nbytes = count * torch.tensor([], dtype=dtype).element_size()
+    return ws[off:off + nbytes].view(dtype)

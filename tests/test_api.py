@@ -1,0 +1,97 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, and rejects bad arguments on the host before anything is
+enqueued (so the fake device addresses below are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from masked_attention_backward_gb300 import binding as mab
+from masked_attention_backward_gb300.workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# Aligned addresses that are never touched: every call below fails validation first.
+FAKE = ctypes.c_void_p(0x7F0000000000)
+MISALIGNED = ctypes.c_void_p(0x7F0000000008)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return mab.load()
+
+
+def _shape(B=1, Hq=4, Hkv=2, Sq=256, Skv=256, D=128, dtype=mab.ATTN_BF16):
+    return mab.attn_shape_t(B, Hq, Hkv, Sq, Skv, D, dtype)
+
+
+def test_exports_every_declared_symbol(lib):
+    hdr = open(os.path.join(ROOT, "include", "maskattn.h")).read()
+    declared = set(re.findall(r"^\s*(?:attn_status_t|const char\*)\s+(attn_\w+)\s*\(", hdr, re.M))
+    assert declared == set(mab.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED",
+                                 "ATTN_ERR_WORKSPACE", "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT"]):
+        assert mab.attn_status_string(code) == name
+
+
+@pytest.mark.parametrize("shape,mask,want", [
+    (_shape(D=64), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_UNSUPPORTED),
+    (_shape(Hq=6, Hkv=4), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(Sq=0), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(Sq=100, Skv=120), mab.attn_mask_desc_t(1, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(), mab.attn_mask_desc_t(2, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(), mab.attn_mask_desc_t(3, 0, 0, 16, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(), mab.attn_mask_desc_t(7, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(dtype=5), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(B=1024, Hq=128, Hkv=128), mab.attn_mask_desc_t(0, 0, 1, 1, None),
+     mab.ATTN_ERR_INVALID_ARG),
+])
+def test_workspace_size_validation(lib, shape, mask, want):
+    r, _ = mab.attn_workspace_size(shape, mask)
+    assert r == want
+
+
+def test_workspace_size_matches_layout(lib):
+    from parity import ws_layout
+    for wl in WORKLOADS:
+        shape = mab.attn_shape_t(wl.B, wl.Hq, wl.Hkv, wl.Sq, wl.Skv, wl.D,
+                                 mab.ATTN_F16 if wl.dtype == "f16" else mab.ATTN_BF16)
+        mask = mab.attn_mask_desc_t(wl.mask_kind, wl.window, wl.bx, wl.by, None)
+        r, n = mab.attn_workspace_size(shape, mask)
+        assert r == mab.ATTN_OK
+        assert n == ws_layout(wl)["total"], wl.name
+
+
+def _bwd(shape, mask, ws_bytes=1 << 30, **over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, dO=FAKE, lse=FAKE, sink=None, dq=FAKE, dk=FAKE,
+                dv=FAKE, dsink=None, ws=FAKE)
+    args.update(over)
+    return mab.attn_bwd(shape, args["q"], args["k"], args["v"], args["o"], args["dO"], args["lse"],
+                        args["sink"], mask, 0.088, args["dq"], args["dk"], args["dv"],
+                        args["dsink"], args["ws"], ws_bytes, None)
+
+
+def test_bwd_argument_errors(lib):
+    shape, mask = _shape(), mab.attn_mask_desc_t(1, 0, 1, 1, None)
+    assert _bwd(shape, mask, q=None) == mab.ATTN_ERR_INVALID_ARG
+    assert _bwd(shape, mask, dv=None) == mab.ATTN_ERR_INVALID_ARG
+    assert _bwd(shape, mask, q=MISALIGNED) == mab.ATTN_ERR_INVALID_ARG
+    assert _bwd(shape, mask, sink=FAKE, dsink=None) == mab.ATTN_ERR_INVALID_ARG
+    assert _bwd(shape, mask, ws_bytes=1024) == mab.ATTN_ERR_WORKSPACE
+    assert _bwd(_shape(D=64), mask) == mab.ATTN_ERR_UNSUPPORTED
+    blk = mab.attn_mask_desc_t(3, 0, 16, 16, None)
+    assert _bwd(shape, blk) == mab.ATTN_ERR_INVALID_ARG  # block mask pointer missing
+
+
+def test_fwd_argument_errors(lib):
+    shape, mask = _shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None)
+    r = mab.attn_fwd(shape, FAKE, FAKE, None, None, mask, 0.088, FAKE, FAKE, FAKE, 1 << 30, None)
+    assert r == mab.ATTN_ERR_INVALID_ARG
+    r = mab.attn_fwd(shape, FAKE, FAKE, FAKE, None, mask, 0.088, FAKE, FAKE, FAKE, 16, None)
+    assert r == mab.ATTN_ERR_WORKSPACE

@@ -1,0 +1,152 @@
+"""GPU parity of attn_bwd against the fp64 oracle, element by element.
+
+Sizes span several tiles of both walks (128-row key tiles with 64-row query
+sub-tiles; 128-row query tiles with 64-row key sub-tiles) and end on ragged
+tails; every mask family of the workloads appears, in both dtypes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from masked_attention_backward_gb300.workloads import (MASK_BLOCK, MASK_CAUSAL, MASK_NONE,
+                                                        MASK_SLIDING, WORKLOADS, Workload,
+                                                        make_inputs)
+from parity import (compare, forward_stats, full_parity, oracle_problem, run_gpu_bwd, ws_layout,
+                    ws_view)
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    WORKLOADS[0],  # the tiny workload exactly: fp16 B1 Hq2 Hkv1 S256 window 64 + sink
+    Workload("swa_sink_bf16_ragged", "bf16", B=2, Hq=4, Hkv=2, Sq=333, Skv=333,
+             mask_kind=MASK_SLIDING, window=100, sink=True, seed=11),
+    Workload("causal_sink_bf16_gqa8", "bf16", B=1, Hq=8, Hkv=1, Sq=515, Skv=515,
+             mask_kind=MASK_CAUSAL, sink=True, seed=12),
+    Workload("causal_f16_nosink", "f16", B=1, Hq=2, Hkv=2, Sq=300, Skv=300,
+             mask_kind=MASK_CAUSAL, seed=13),
+    Workload("random_blocks_f16", "f16", B=1, Hq=2, Hkv=2, Sq=700, Skv=700, mask_kind=MASK_BLOCK,
+             bx=64, by=64, block_pattern="random", density=0.3, seed=14),
+    Workload("bigbird_f16_uneven", "f16", B=2, Hq=2, Hkv=2, Sq=500, Skv=700, mask_kind=MASK_BLOCK,
+             bx=48, by=80, block_pattern="bigbird", seed=15),
+    Workload("blocks_bf16_small_bxby", "bf16", B=1, Hq=4, Hkv=2, Sq=257, Skv=190,
+             mask_kind=MASK_BLOCK, bx=16, by=32, block_pattern="random", density=0.2, sink=True,
+             seed=16),
+    Workload("dense_f16_uneven", "f16", B=1, Hq=2, Hkv=1, Sq=200, Skv=333, mask_kind=MASK_NONE,
+             seed=17),
+    Workload("dense_bf16_sink", "bf16", B=2, Hq=2, Hkv=2, Sq=129, Skv=129, mask_kind=MASK_NONE,
+             sink=True, seed=18),
+]
+
+
+@pytest.mark.parametrize("wl", CASES, ids=[w.name for w in CASES])
+def test_bwd_parity(cuda_lib, wl):
+    reps, _, _ = full_parity(wl)
+    print({r["name"]: (round(r["frac"], 6), r["max_err"]) for r in reps})
+
+
+@pytest.mark.parametrize("S", [1, 2, 63, 64, 65, 127, 128, 129])
+def test_bwd_tiny_lengths(cuda_lib, S):
+    wl = Workload(f"causal_sink_S{S}", "bf16", B=1, Hq=4, Hkv=1, Sq=S, Skv=S,
+                  mask_kind=MASK_CAUSAL, sink=True, seed=20 + S)
+    full_parity(wl)
+
+
+def test_bwd_sink_minus_inf_matches_no_sink(cuda_lib):
+    wl = Workload("swa_f16", "f16", B=1, Hq=2, Hkv=1, Sq=200, Skv=200, mask_kind=MASK_SLIDING,
+                  window=50, sink=True, seed=30)
+    inp = make_inputs(wl)
+    inp.sink = torch.full((wl.Hq,), float("-inf"))
+    pb = oracle_problem(wl, inp)
+    O, lse = forward_stats(wl, inp, pb)
+    run = run_gpu_bwd(wl, inp, O, lse)
+    ref = oracle.backward(pb, inp.q, inp.k, inp.v, O, inp.dO, lse)
+    for name in ("dq", "dk", "dv"):
+        compare(name, getattr(run, name), ref[name], wl.dtype)
+    assert torch.all(run.dsink.cpu() == 0)
+
+
+def test_bwd_empty_rows_and_empty_key_tiles(cuda_lib):
+    # head 1 has whole query blocks and whole key blocks switched off: rows that
+    # see nothing get dQ = 0, key tiles that nobody sees get dK = dV = 0
+    wl = Workload("holes_f16", "f16", B=1, Hq=2, Hkv=2, Sq=400, Skv=400, mask_kind=MASK_BLOCK,
+                  bx=64, by=64, block_pattern="ones", seed=31)
+    inp = make_inputs(wl)
+    inp.block_mask[0, 1, 2, :] = 0      # query rows 128..191 of head 1 see nothing
+    inp.block_mask[0, 1, :, 4:] = 0     # keys 256.. of head 1 are seen by nobody
+    inp.block_mask[0, 0, :, :] = 0      # head 0: nothing at all
+    pb = oracle_problem(wl, inp)
+    O, lse = forward_stats(wl, inp, pb)
+    run = run_gpu_bwd(wl, inp, O, lse)
+    ref = oracle.backward(pb, inp.q, inp.k, inp.v, O, inp.dO, lse)
+    for name in ("dq", "dk", "dv"):
+        compare(name, getattr(run, name), ref[name], wl.dtype)
+    assert torch.all(run.dq[0, 1, 128:192].cpu() == 0)
+    assert torch.all(run.dq[0, 0].cpu() == 0)
+    assert torch.all(run.dk[0, 1, 256:].cpu() == 0) and torch.all(run.dv[0, 1, 256:].cpu() == 0)
+    assert torch.all(run.dk[0, 0].cpu() == 0)
+
+
+def test_bwd_extreme_logits_fp16(cuda_lib):
+    # a few q entries near +-32000 in fp16 keep every logit finite in fp32
+    wl = Workload("big_f16", "f16", B=1, Hq=2, Hkv=1, Sq=130, Skv=130, mask_kind=MASK_CAUSAL,
+                  sink=True, seed=32)
+    inp = make_inputs(wl)
+    spikes = (torch.rand(inp.q.shape, generator=torch.Generator().manual_seed(5)) < 0.01)
+    inp.q = torch.where(spikes, inp.q.float().sign() * 32000, inp.q.float()).half()
+    pb = oracle_problem(wl, inp)
+    O, lse = forward_stats(wl, inp, pb)
+    run = run_gpu_bwd(wl, inp, O, lse)
+    for t in (run.dq, run.dk, run.dv):
+        assert torch.isfinite(t.float()).all()
+
+
+def test_bwd_deterministic(cuda_lib):
+    wl = CASES[4]
+    inp = make_inputs(wl)
+    O, lse = forward_stats(wl, inp)
+    a = run_gpu_bwd(wl, inp, O, lse)
+    for _ in range(3):
+        b = run_gpu_bwd(wl, inp, O, lse)
+        for name in ("dq", "dk", "dv"):
+            assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+@pytest.mark.parametrize("wl", [CASES[4], CASES[5], CASES[6]], ids=lambda w: w.name)
+def test_tables_bit_exact(cuda_lib, wl):
+    inp = make_inputs(wl)
+    O, lse = forward_stats(wl, inp)
+    run = run_gpu_bwd(wl, inp, O, lse)
+    L = ws_layout(wl)
+    assert run.ws.numel() == L["total"]
+    BH = wl.B * wl.Hq
+    ws = run.ws.cpu()
+    maskT = ws_view(ws, L["maskT"], BH * wl.nqb * wl.nkb, torch.uint8).numpy()
+    want = oracle.mask_transpose(inp.block_mask.numpy())
+    assert np.array_equal(maskT.reshape(want.shape), want)
+    sel_k, cnt_k, sel_q, cnt_q = oracle.select_tables(inp.block_mask.numpy(), wl.Sq, wl.Skv, wl.bx,
+                                                      wl.by, 64, 128, 128, 64)
+    g_sel_k = ws_view(ws, L["sel_k"], sel_k.size, torch.int32).numpy().reshape(sel_k.shape)
+    g_cnt_k = ws_view(ws, L["cnt_k"], cnt_k.size, torch.int32).numpy().reshape(cnt_k.shape)
+    g_sel_q = ws_view(ws, L["sel_q"], sel_q.size, torch.int32).numpy().reshape(sel_q.shape)
+    g_cnt_q = ws_view(ws, L["cnt_q"], cnt_q.size, torch.int32).numpy().reshape(cnt_q.shape)
+    assert np.array_equal(g_cnt_k, cnt_k) and np.array_equal(g_sel_k, sel_k)
+    assert np.array_equal(g_cnt_q, cnt_q) and np.array_equal(g_sel_q, sel_q)
+
+
+def test_preprocess_delta_and_lse2(cuda_lib):
+    wl = CASES[1]
+    inp = make_inputs(wl)
+    pb = oracle_problem(wl, inp)
+    O, lse = forward_stats(wl, inp, pb)
+    run = run_gpu_bwd(wl, inp, O, lse)
+    L = ws_layout(wl)
+    BH, Sp = wl.B * wl.Hq, L["Sq_pad"]
+    ws = run.ws.cpu()
+    delta = ws_view(ws, L["delta"], BH * Sp, torch.float32).reshape(BH, Sp).double().numpy()
+    lse2 = ws_view(ws, L["lse2"], BH * Sp, torch.float32).reshape(BH, Sp).double().numpy()
+    ref = oracle.delta(pb, O, inp.dO).reshape(BH, wl.Sq)
+    assert np.all(np.abs(delta[:, :wl.Sq] - ref) <= 1e-5 * (1 + np.abs(ref)))
+    assert np.all(delta[:, wl.Sq:] == 0) and np.all(np.isposinf(lse2[:, wl.Sq:]))
+    want = lse.double().numpy().reshape(BH, wl.Sq) * np.log2(np.e)
+    assert np.all(np.abs(lse2[:, :wl.Sq] - want) <= 1e-6 * (1 + np.abs(want)))
