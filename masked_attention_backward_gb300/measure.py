@@ -1,0 +1,57 @@
+"""Work units of the backward pass, for throughput reporting.
+
+The unit is a visible (b, h, i, j) token pair.  The count does not depend on
+the kernels' tile sizes, so work spent on masked positions inside partially
+visible tiles earns no credit.  Per visible pair the five contractions of the
+backward (S = QK^T, dP = dO V^T, dV += P^T dO, dK += dS^T Q, dQ += dS K) cost
+2*D flops each:
+
+  end-to-end         10 * D * pairs
+  dK/dV kernel        8 * D * pairs   (S, dP, dV, dK)
+  dQ kernel           6 * D * pairs   (S, dP, dQ; S and dP are recomputed)
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .workloads import MASK_BLOCK, MASK_CAUSAL, MASK_NONE, MASK_SLIDING, Workload
+
+
+def visible_pairs(wl: Workload, block_mask=None) -> int:
+    heads = wl.B * wl.Hq
+    S = wl.Sq
+    if wl.mask_kind == MASK_NONE:
+        return heads * wl.Sq * wl.Skv
+    if wl.mask_kind == MASK_CAUSAL:
+        return heads * S * (S + 1) // 2
+    if wl.mask_kind == MASK_SLIDING:
+        W = wl.window
+        if W >= S:
+            return heads * S * (S + 1) // 2
+        return heads * (W * (W + 1) // 2 + (S - W) * W)
+    if wl.mask_kind == MASK_BLOCK:
+        m = np.asarray(block_mask.cpu().numpy() if hasattr(block_mask, "cpu") else block_mask,
+                       dtype=np.int64)
+        rows = np.minimum(wl.bx, wl.Sq - np.arange(wl.nqb) * wl.bx)
+        cols = np.minimum(wl.by, wl.Skv - np.arange(wl.nkb) * wl.by)
+        return int(np.einsum("bhqk,q,k->", m, rows, cols))
+    raise ValueError(wl.mask_kind)
+
+
+def flops(wl: Workload, pairs: int) -> dict:
+    D = wl.D
+    return {"total": 10 * D * pairs, "dkdv": 8 * D * pairs, "dq": 6 * D * pairs}
+
+
+def algorithmic_bytes(wl: Workload, block_mask_bytes: int = 0) -> dict:
+    """Bytes each tensor must cross HBM once: q, k, v, o, dO, lse read; dq, dk,
+    dv written (plus sink / dsink and the block mask)."""
+    e = 2
+    q = wl.B * wl.Hq * wl.Sq * wl.D * e
+    kv = wl.B * wl.Hkv * wl.Skv * wl.D * e
+    lse = wl.B * wl.Hq * wl.Sq * 4
+    read = 3 * q + 2 * kv + lse + block_mask_bytes
+    write = q + 2 * kv
+    return {"read": read, "write": write, "total": read + write,
+            # preprocess alone: reads o, dO, lse; writes Delta and lse*log2(e)
+            "preprocess": 2 * q + lse + 2 * lse}

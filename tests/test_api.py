@@ -95,3 +95,23 @@ def test_fwd_argument_errors(lib):
     assert r == mab.ATTN_ERR_INVALID_ARG
     r = mab.attn_fwd(shape, FAKE, FAKE, FAKE, None, mask, 0.088, FAKE, FAKE, FAKE, 16, None)
     assert r == mab.ATTN_ERR_WORKSPACE
+
+
+def test_visible_pair_count_matches_oracle():
+    import numpy as np
+    import oracle
+    from masked_attention_backward_gb300 import measure
+    from masked_attention_backward_gb300.workloads import Workload, make_inputs
+    cases = [Workload("c", "f16", 2, 3, 1, 37, 37, 8, mask_kind=1),
+             Workload("s", "f16", 1, 2, 2, 41, 41, 8, mask_kind=2, window=6),
+             Workload("s2", "f16", 1, 2, 2, 5, 5, 8, mask_kind=2, window=9),
+             Workload("n", "f16", 1, 2, 1, 13, 29, 8, mask_kind=0),
+             Workload("b", "f16", 2, 2, 2, 50, 70, 8, mask_kind=3, bx=6, by=9,
+                      block_pattern="random", density=0.4, seed=3)]
+    for wl in cases:
+        inp = make_inputs(wl)
+        pb = oracle.Problem(B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, Sq=wl.Sq, Skv=wl.Skv, D=wl.D,
+                            scale=wl.scale, mask_kind=wl.mask_kind, window=wl.window, bx=wl.bx,
+                            by=wl.by, block_mask=None if inp.block_mask is None
+                            else inp.block_mask.numpy())
+        assert measure.visible_pairs(wl, inp.block_mask) == oracle.count_visible(pb), wl.name
