@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Throughput of the masked attention backward on GB300.
+
+One step = one attn_bwd call (preprocess, dK/dV, dQ, dSink; plus the mask
+tables for block masks) over the workload's full problem, inputs resident in
+HBM.  The L2 cache is flushed (a 512 MiB device write) before every timed
+step, outside the timed events.  Throughput counts 10*D flops per visible
+(b, h, i, j) pair (the five contractions of the backward), so work spent on
+masked positions inside partially visible tiles earns nothing.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+With N > 1 (launched by torch.distributed.run) every rank runs its own full
+copy of the workload (weak scaling: the backward has no exchange step) and the
+time is the maximum over ranks.  Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from masked_attention_backward_gb300 import measure  # noqa: E402
+from masked_attention_backward_gb300.workloads import BY_NAME, make_inputs  # noqa: E402
+
+METRIC = "attn bwd TFLOP/s over unmasked tiles & ms/call; % of GB300 BF16 tensor peak"
+DEFAULT_WORKLOAD = "gqa_sink_causal_s16384"
+MASK_NAMES = {0: "none", 1: "causal", 2: "causal+sliding window", 3: "block"}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Files whose content decides the dK/dV and dQ kernels' DRAM traffic.
+KERNEL_SOURCES = {
+    "k_dkdv": ["csrc/attn_kv.cu", "csrc/tiles.cuh", "csrc/ptx.cuh", "csrc/internal.h"],
+    "k_dq": ["csrc/attn_q.cu", "csrc/tiles.cuh", "csrc/ptx.cuh", "csrc/internal.h"],
+}
+
+
+def kernel_hash(name: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES.get(name, []):
+        with open(os.path.join(ROOT, "masked_attention_backward_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        uuid = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+        except Exception:
+            pass
+        rows = []
+        for line in self.out.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 10:
+                rows.append(parts)
+        if uuid:
+            mine = [r for r in rows if uuid.replace("GPU-", "") in r[1]]
+            rows = mine or rows
+        idx = {r[0] for r in rows}
+        if len(idx) > 1:
+            rows = [r for r in rows if r[0] == sorted(idx)[0]]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[2]) for r in rows if num(r[2]) is not None]
+        smax = [num(r[3]) for r in rows if num(r[3]) is not None]
+        power = [num(r[4]) for r in rows if num(r[4]) is not None]
+        reasons = set()
+        for r in rows:
+            for name, col in (("hw_slowdown", 6), ("hw_thermal_slowdown", 7),
+                              ("sw_thermal_slowdown", 8), ("sw_power_cap", 9)):
+                if "Active" in r[col] and "Not" not in r[col]:
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def gpu_inputs(wl, device):
+    from masked_attention_backward_gb300 import binding as mab
+    inp = make_inputs(wl)
+    q, k, v, dO = (t.to(device) for t in (inp.q, inp.k, inp.v, inp.dO))
+    sink = inp.sink.to(device) if inp.sink is not None else None
+    bm = inp.block_mask.to(device) if inp.block_mask is not None else None
+    mask = mab.Mask(kind=wl.mask_kind, window=wl.window, bx=wl.bx, by=wl.by, block_mask=bm)
+    o, lse = mab.fwd(q, k, v, sink, mask, wl.scale)   # O and LSE from the CUDA forward
+    torch.cuda.synchronize()
+    return inp, dict(q=q, k=k, v=v, o=o, dO=dO, lse=lse, sink=sink, mask=mask)
+
+
+def run_ours(args, rank, world, local):
+    from masked_attention_backward_gb300 import binding as mab
+    mab.load()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    wl = BY_NAME[args.workload]
+    inp, t = gpu_inputs(wl, device)
+    pairs = measure.visible_pairs(wl, inp.block_mask)
+    fl = measure.flops(wl, pairs)
+    ws = mab.workspace(mab.shape_of(t["q"], t["k"]), t["mask"], device)
+    dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
+    dsink = torch.empty_like(t["sink"]) if t["sink"] is not None else None
+    out = (dq, dk, dv, dsink)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+
+    def step():
+        mab.bwd(t["q"], t["k"], t["v"], t["o"], t["dO"], t["lse"], t["sink"], t["mask"],
+                wl.scale, ws=ws, out=out)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    status = mab.device_status(ws)
+    if status != mab.ATTN_OK:
+        raise RuntimeError("device status after warm-up: " + mab.attn_status_string(status))
+
+    # ---- device-timed steps, per-kernel events from the library
+    mab.attn_profile_enable(True)
+    clocks = ClockSampler(local).start()
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    step_ms, kern = [], {}
+    launches = 0
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+        prof = mab.attn_profile_read()
+        launches += len(prof)
+        for name, ms in prof:
+            kern.setdefault(name, []).append(ms)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    mab.attn_profile_enable(False)
+    status = mab.device_status(ws)
+    if status != mab.ATTN_OK:
+        raise RuntimeError("device status after timing: " + mab.attn_status_string(status))
+    t_rank = float(sum(step_ms))
+    t_max = max_over_ranks(t_rank, world, device)
+    ms_per_step = t_max / args.steps
+    value = world * fl["total"] * args.steps / (t_max * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "o", "dO", "lse")}
+        if t["sink"] is not None:
+            host_in["sink"] = t["sink"].cpu().pin_memory()
+        host_out = [x.cpu().pin_memory() for x in out if x is not None]
+        dev_in = {n: torch.empty_like(t[n]) for n in host_in}
+        h2d = sum(x.numel() * x.element_size() for x in host_in.values())
+        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        e2e_ms = []
+        for it in range(args.warmup + args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for n, h in host_in.items():
+                dev_in[n].copy_(h, non_blocking=True)
+            mab.bwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["o"], dev_in["dO"],
+                    dev_in["lse"], dev_in.get("sink"), t["mask"], wl.scale, ws=ws, out=out)
+            for h, d in zip(host_out, [x for x in out if x is not None]):
+                h.copy_(d, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if it >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+        te = max_over_ranks(float(sum(e2e_ms)), world, device)
+        e2e = {"value": round(world * fl["total"] * args.steps / (te * 1e-3) / 1e12, 2),
+               "unit": "TFLOP/s", "ms_per_step": round(te / args.steps, 3),
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    # ---- roofline of the dominant kernel
+    peaks, peak_src = load_peaks()
+    avg = {n: float(np.mean(v)) for n, v in kern.items()}
+    dom = max(("k_dkdv", "k_dq"), key=lambda n: avg.get(n, 0.0))
+    dom_flops = fl["dkdv"] if dom == "k_dkdv" else fl["dq"]
+    achieved = dom_flops / (avg[dom] * 1e-3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops")
+    if wl.dtype == "f16":
+        peak = peak  # fp16 and bf16 share the dense tensor rate
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tr = json.load(f)
+        ent = tr.get(args.workload, {}).get(dom)
+        if ent and ent.get("source_hash") == kernel_hash(dom):
+            traffic = ent.get("bytes_per_launch")
+    kernels = {}
+    for n, a in avg.items():
+        d = {"ms": round(a, 4), "share": round(sum(kern[n]) / sum(sum(v) for v in kern.values()), 4)}
+        if n == "k_dkdv":
+            d["tflops"] = round(fl["dkdv"] / (a * 1e-3) / 1e12, 1)
+        elif n == "k_dq":
+            d["tflops"] = round(fl["dq"] / (a * 1e-3) / 1e12, 1)
+        elif n == "k_preprocess":
+            d["gbps"] = round(measure.algorithmic_bytes(wl)["preprocess"] / (a * 1e-3) / 1e9, 1)
+        kernels[n] = d
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, inp, fl, budget_s=args.cpu_seconds)
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype, "data": "synthetic",
+        "config": workload_config(wl, pairs, fl),
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside "
+                                    f"a seconds-long loop)",
+                     "flops_per_launch": dom_flops},
+        "kernels": kernels,
+        "pct_of_peak_end_to_end": round(value / world / peak, 4),
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
+def workload_config(wl, pairs, fl):
+    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "Sq": wl.Sq,
+            "Skv": wl.Skv, "D": wl.D, "mask": MASK_NAMES[wl.mask_kind],
+            "window": wl.window or None, "bx": wl.bx if wl.mask_kind == 3 else None,
+            "by": wl.by if wl.mask_kind == 3 else None, "sink": wl.sink,
+            "visible_pairs": int(pairs), "flops_per_step": int(fl["total"]),
+            "l2": "flushed before every step (512 MiB device write, outside the timed events)",
+            "o_lse_source": "CUDA forward (attn_fwd) on the same inputs"}
+
+
+def cpu_baseline(wl, inp, fl, budget_s: float = 15.0, seed: int = 0):
+    """Time the fp64 oracle on a bounded random sample of query rows (dQ) and
+    key rows (dK, dV) of the workload and extrapolate to one full call.
+
+    The oracle's cost per row does not depend on the values of O and LSE, so
+    the sample runs with placeholder statistics (LSE = 0, Delta = 0)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    pb = oracle.Problem(B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, Sq=wl.Sq, Skv=wl.Skv, D=wl.D,
+                        scale=wl.scale, mask_kind=wl.mask_kind, window=wl.window, bx=wl.bx,
+                        by=wl.by,
+                        block_mask=None if inp.block_mask is None else inp.block_mask.numpy(),
+                        sink=None if inp.sink is None else inp.sink.double().numpy())
+    q = inp.q.double().numpy()
+    k = inp.k.double().numpy()
+    v = inp.v.double().numpy()
+    dO = inp.dO.double().numpy()
+    lse = np.zeros((wl.B, wl.Hq, wl.Sq))
+    dl = np.zeros((wl.B, wl.Hq, wl.Sq))
+    nrows, ncols = wl.B * wl.Hq * wl.Sq, wl.B * wl.Hkv * wl.Skv
+    per = {"rows": 0.0, "cols": 0.0}
+    counts = {"rows": 0, "cols": 0}
+    n = 4
+    t_start = time.perf_counter()
+    while True:
+        rows = rng.integers(0, nrows, size=n)
+        cols = rng.integers(0, ncols, size=max(1, n // 8))
+        t0 = time.perf_counter()
+        oracle.dq_rows(pb, q, k, v, dO, lse, dl, rows)
+        t1 = time.perf_counter()
+        oracle.dkdv_cols(pb, q, k, v, dO, lse, dl, cols)
+        t2 = time.perf_counter()
+        per["rows"] += t1 - t0
+        per["cols"] += t2 - t1
+        counts["rows"] += rows.size
+        counts["cols"] += cols.size
+        spent = time.perf_counter() - t_start
+        if spent >= budget_s:
+            break
+        n = int(min(n * 2, max(4, n * (budget_s - spent) / max(t2 - t0, 1e-3))))
+    est = per["rows"] / counts["rows"] * nrows + per["cols"] / counts["cols"] * ncols
+    return {"value": round(fl["total"] / est / 1e12, 6), "unit": "TFLOP/s",
+            "ms_per_call": round(est * 1e3, 1), "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{counts['rows']} random query rows (dQ) and {counts['cols']} random key "
+                      f"rows (dK, dV) of {wl.name}, fp64, {round(time.perf_counter() - t_start, 1)}"
+                      f" s of CPU time, extrapolated to the full call by row counts"}
+
+
+def run_reference(args, rank, world):
+    """The fp64 oracle as the reference arm: rank 0 only, host cores."""
+    if rank != 0:
+        return None
+    wl = BY_NAME[args.workload]
+    inp = make_inputs(wl)
+    pairs = measure.visible_pairs(wl, inp.block_mask)
+    fl = measure.flops(wl, pairs)
+    per_step = max(2.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup):
+        cpu_baseline(wl, inp, fl, budget_s=per_step / 4, seed=100 + i)
+    ests = [cpu_baseline(wl, inp, fl, budget_s=per_step, seed=i) for i in range(args.steps)]
+    ms = float(np.mean([e["ms_per_call"] for e in ests]))
+    value = fl["total"] / (ms * 1e-3) / 1e12
+    cpu = dict(ests[-1])
+    cpu["value"] = round(value, 6)
+    cpu["sample"] = f"{args.steps} timed samples; last: " + cpu["sample"]
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, pairs, fl), "cpu_baseline": cpu,
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(BY_NAME))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

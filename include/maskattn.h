@@ -120,6 +120,18 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
  * wait ran out.  ATTN_ERR_CUDA if the synchronization itself fails. */
 attn_status_t attn_get_device_status(const void* ws, void* stream);
 
+/* Per-kernel timing, for diagnostics and benchmarks.  attn_profile_enable(1)
+ * makes later attn_fwd / attn_bwd calls on this process bracket every kernel
+ * they enqueue with CUDA events (created on first use, on the current device,
+ * and kept until the process exits); attn_profile_enable(0) stops it.
+ * attn_profile_read waits for the events of the most recent profiled call and
+ * writes up to `capacity` kernel names (static strings) and elapsed times in
+ * milliseconds, in launch order; *count receives the number of kernels.
+ * Errors: ATTN_ERR_INVALID_ARG (null count, or names/ms null with capacity >
+ * 0), ATTN_ERR_CUDA (event creation or synchronization failed). */
+attn_status_t attn_profile_enable(int on);
+attn_status_t attn_profile_read(const char** names, float* ms, int capacity, int* count);
+
 /* Static string naming a status code ("ATTN_OK", ...). Never NULL. */
 const char* attn_status_string(attn_status_t status);
 

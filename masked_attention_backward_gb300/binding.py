@@ -22,7 +22,7 @@ ATTN_MASK_NONE, ATTN_MASK_CAUSAL, ATTN_MASK_SLIDING, ATTN_MASK_BLOCK = range(4)
 
 # Every symbol include/maskattn.h declares.
 EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_get_device_status",
-           "attn_status_string")
+           "attn_profile_enable", "attn_profile_read", "attn_status_string")
 
 
 class attn_shape_t(ctypes.Structure):
@@ -64,6 +64,12 @@ def load(build: bool = True) -> ctypes.CDLL:
             lib.attn_bwd.restype = ctypes.c_int
             lib.attn_get_device_status.argtypes = [vp, vp]
             lib.attn_get_device_status.restype = ctypes.c_int
+            lib.attn_profile_enable.argtypes = [ctypes.c_int]
+            lib.attn_profile_enable.restype = ctypes.c_int
+            lib.attn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_char_p),
+                                              ctypes.POINTER(ctypes.c_float), ctypes.c_int,
+                                              ctypes.POINTER(ctypes.c_int)]
+            lib.attn_profile_read.restype = ctypes.c_int
             lib.attn_status_string.argtypes = [ctypes.c_int]
             lib.attn_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -95,6 +101,21 @@ def attn_bwd(shape, q, k, v, o, dO, lse, sink, mask, scale, dq, dk, dv, dsink, w
 
 def attn_get_device_status(ws, stream) -> int:
     return load().attn_get_device_status(ws, stream)
+
+
+def attn_profile_enable(on: bool) -> int:
+    return load().attn_profile_enable(1 if on else 0)
+
+
+def attn_profile_read(capacity: int = 16):
+    """[(kernel name, ms)] of the most recent profiled call."""
+    names = (ctypes.c_char_p * capacity)()
+    ms = (ctypes.c_float * capacity)()
+    n = ctypes.c_int(0)
+    r = load().attn_profile_read(names, ms, capacity, ctypes.byref(n))
+    if r != ATTN_OK:
+        raise AttnError(r, "attn_profile_read")
+    return [(names[i].decode(), float(ms[i])) for i in range(min(n.value, capacity))]
 
 
 # ------------------------------------------------------------- torch helpers

@@ -15,6 +15,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "../../include/maskattn.h"
 #include "internal.h"
 #include "tmap.h"
@@ -156,6 +158,41 @@ AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const W
 
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
+// ---- optional per-kernel events (attn_profile_enable) ----
+struct Profiler {
+  static constexpr int kMax = 16;
+  std::mutex mu;
+  bool on = false;
+  bool created = false;
+  int device = -1;
+  cudaEvent_t ev[kMax][2];
+  const char* names[kMax];
+  int n = 0;
+};
+Profiler g_prof;
+
+// Brackets one launch with events when profiling is on.
+struct ProfScope {
+  cudaStream_t st;
+  bool active;
+  int slot;
+  ProfScope(const char* name, cudaStream_t s) : st(s), active(false), slot(-1) {
+    if (!g_prof.on || !g_prof.created || g_prof.n >= Profiler::kMax) return;
+    slot = g_prof.n++;
+    g_prof.names[slot] = name;
+    active = cudaEventRecord(g_prof.ev[slot][0], st) == cudaSuccess;
+  }
+  ~ProfScope() {
+    if (active) cudaEventRecord(g_prof.ev[slot][1], st);
+  }
+};
+
+// Called at the start of every profiled API call.
+void prof_begin() {
+  if (!g_prof.on) return;
+  g_prof.n = 0;
+}
+
 // Transposed mask and both select tables (block masks only).
 cudaError_t enqueue_tables(const attn_shape_t* sh, const WsLayout& L, uint8_t* ws,
                            const AttnParams& p, cudaStream_t st) {
@@ -216,9 +253,17 @@ attn_status_t attn_fwd(const attn_shape_t* shape, const void* q, const void* k, 
       !make_bhsd_map(&tK, k, bf16, BHkv, shape->Skv, Q_SUB) ||
       !make_bhsd_map(&tV, v, bf16, BHkv, shape->Skv, Q_SUB))
     return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  prof_begin();
   cudaError_t e = cudaMemsetAsync(w + L.status, 0, sizeof(DevStatus), st);
-  if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) e = enqueue_tables(shape, L, w, p, st);
-  if (e == cudaSuccess) e = launch_fwd(bf16, p, tQ, tK, tV, o, st);
+  if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) {
+    ProfScope ps("k_mask_tables", st);
+    e = enqueue_tables(shape, L, w, p, st);
+  }
+  if (e == cudaSuccess) {
+    ProfScope ps("k_attn_fwd", st);
+    e = launch_fwd(bf16, p, tQ, tK, tV, o, st);
+  }
   return cuda_status(e);
 }
 
@@ -257,18 +302,33 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
       !make_bhsd_map(&tVs, v, bf16, BHkv, shape->Skv, Q_SUB))
     return ATTN_ERR_CUDA;
 
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  prof_begin();
   cudaError_t e = cudaMemsetAsync(w + L.status, 0, sizeof(DevStatus), st);
-  if (e == cudaSuccess)
+  if (e == cudaSuccess) {
+    ProfScope ps("k_preprocess", st);
     e = launch_preprocess(bf16, o, dO, lse, sink, reinterpret_cast<float*>(w + L.lse2),
                           reinterpret_cast<float*>(w + L.delta),
                           reinterpret_cast<float*>(w + L.dsink_part), shape->B, shape->Hq,
                           shape->Sq, d.Sq_pad, st);
-  if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) e = enqueue_tables(shape, L, w, p, st);
-  if (e == cudaSuccess) e = launch_dkdv(bf16, p, tQs, tdOs, tKt, tVt, dk, dv, st);
-  if (e == cudaSuccess) e = launch_dq(bf16, p, tQt, tdOt, tKs, tVs, dq, st);
-  if (e == cudaSuccess && sink)
+  }
+  if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) {
+    ProfScope ps("k_mask_tables", st);
+    e = enqueue_tables(shape, L, w, p, st);
+  }
+  if (e == cudaSuccess) {
+    ProfScope ps("k_dkdv", st);
+    e = launch_dkdv(bf16, p, tQs, tdOs, tKt, tVt, dk, dv, st);
+  }
+  if (e == cudaSuccess) {
+    ProfScope ps("k_dq", st);
+    e = launch_dq(bf16, p, tQt, tdOt, tKs, tVs, dq, st);
+  }
+  if (e == cudaSuccess && sink) {
+    ProfScope ps("k_dsink_finalize", st);
     e = launch_dsink_finalize(reinterpret_cast<const float*>(w + L.dsink_part), shape->Hq,
                               d.nparts, dsink, st);
+  }
   return cuda_status(e);
 }
 
@@ -279,6 +339,47 @@ attn_status_t attn_get_device_status(const void* ws, void* stream) {
   DevStatus h;
   if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
   return h.code == 0 ? ATTN_OK : static_cast<attn_status_t>(h.code);
+}
+
+attn_status_t attn_profile_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  if (on) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (g_prof.created && g_prof.device != dev) {
+      for (int i = 0; i < Profiler::kMax; ++i) {
+        cudaEventDestroy(g_prof.ev[i][0]);
+        cudaEventDestroy(g_prof.ev[i][1]);
+      }
+      g_prof.created = false;
+    }
+    if (!g_prof.created) {
+      for (int i = 0; i < Profiler::kMax; ++i)
+        if (cudaEventCreate(&g_prof.ev[i][0]) != cudaSuccess ||
+            cudaEventCreate(&g_prof.ev[i][1]) != cudaSuccess)
+          return ATTN_ERR_CUDA;
+      g_prof.created = true;
+      g_prof.device = dev;
+    }
+  }
+  g_prof.on = on != 0;
+  g_prof.n = 0;
+  return ATTN_OK;
+}
+
+attn_status_t attn_profile_read(const char** names, float* ms, int capacity, int* count) {
+  if (!count || (capacity > 0 && (!names || !ms))) return ATTN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  *count = g_prof.created ? g_prof.n : 0;
+  for (int i = 0; i < *count && i < capacity; ++i) {
+    if (cudaEventSynchronize(g_prof.ev[i][1]) != cudaSuccess) return ATTN_ERR_CUDA;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, g_prof.ev[i][0], g_prof.ev[i][1]) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    names[i] = g_prof.names[i];
+    ms[i] = t;
+  }
+  return ATTN_OK;
 }
 
 }  // extern "C"
