@@ -115,6 +115,22 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
                        const attn_mask_desc_t* mask, float scale, void* dq, void* dk, void* dv,
                        float* dsink, void* ws, size_t ws_bytes, void* stream);
 
+/* Backward for callers that cannot allocate device memory (operator or plugin
+ * interfaces that receive no workspace, services that forbid allocation while
+ * running).  The pages describe no such variant; this is an addition of this
+ * library.  Same arguments and results as attn_bwd, without ws / ws_bytes:
+ * the scratch lives in a fixed 32 MiB device array inside the library, held
+ * on every GPU that loads it until the process exits.  The first call on a
+ * device looks up that array's address (make that first call before any
+ * stream capture on the device).  Errors: those of attn_bwd, and
+ * ATTN_ERR_WORKSPACE when attn_workspace_size() for the shape exceeds 32 MiB.
+ * All calls on a device share the array: calls whose GPU work overlaps in
+ * time race on it and give wrong results, so order them on one stream. */
+attn_status_t attn_bwd_noalloc(const attn_shape_t* shape, const void* q, const void* k,
+                               const void* v, const void* o, const void* dO, const float* lse,
+                               const float* sink, const attn_mask_desc_t* mask, float scale,
+                               void* dq, void* dk, void* dv, float* dsink, void* stream);
+
 /* Synchronizes `stream`, then reads the status word that the last call which
  * used `ws` left in the workspace: ATTN_OK, or ATTN_ERR_TIMEOUT when a device
  * wait ran out.  ATTN_ERR_CUDA if the synchronization itself fails. */

@@ -21,8 +21,9 @@ ATTN_F16, ATTN_BF16 = 0, 1
 ATTN_MASK_NONE, ATTN_MASK_CAUSAL, ATTN_MASK_SLIDING, ATTN_MASK_BLOCK = range(4)
 
 # Every symbol include/maskattn.h declares.
-EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_get_device_status",
-           "attn_profile_enable", "attn_profile_read", "attn_status_string")
+EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_bwd_noalloc",
+           "attn_get_device_status", "attn_profile_enable", "attn_profile_read",
+           "attn_status_string")
 
 
 class attn_shape_t(ctypes.Structure):
@@ -62,6 +63,9 @@ def load(build: bool = True) -> ctypes.CDLL:
             lib.attn_bwd.argtypes = [ps, vp, vp, vp, vp, vp, vp, vp, pm, ctypes.c_float,
                                      vp, vp, vp, vp, vp, sz, vp]
             lib.attn_bwd.restype = ctypes.c_int
+            lib.attn_bwd_noalloc.argtypes = [ps, vp, vp, vp, vp, vp, vp, vp, pm, ctypes.c_float,
+                                             vp, vp, vp, vp, vp]
+            lib.attn_bwd_noalloc.restype = ctypes.c_int
             lib.attn_get_device_status.argtypes = [vp, vp]
             lib.attn_get_device_status.restype = ctypes.c_int
             lib.attn_profile_enable.argtypes = [ctypes.c_int]
@@ -97,6 +101,14 @@ def attn_bwd(shape, q, k, v, o, dO, lse, sink, mask, scale, dq, dk, dv, dsink, w
              stream) -> int:
     return load().attn_bwd(ctypes.byref(shape), q, k, v, o, dO, lse, sink, ctypes.byref(mask),
                            ctypes.c_float(scale), dq, dk, dv, dsink, ws, ws_bytes, stream)
+
+
+def attn_bwd_noalloc(shape, q, k, v, o, dO, lse, sink, mask, scale, dq, dk, dv, dsink,
+                     stream) -> int:
+    """attn_bwd with the library's fixed device scratch instead of a workspace."""
+    return load().attn_bwd_noalloc(ctypes.byref(shape), q, k, v, o, dO, lse, sink,
+                                   ctypes.byref(mask), ctypes.c_float(scale), dq, dk, dv, dsink,
+                                   stream)
 
 
 def attn_get_device_status(ws, stream) -> int:
