@@ -80,7 +80,13 @@ WORKLOADS = [
     Workload("gqa_sink_causal_s16384", "bf16", B=1, Hq=64, Hkv=8, Sq=16384, Skv=16384,
              mask_kind=MASK_CAUSAL, sink=True, seed=4),
 ]
-BY_NAME = {w.name: w for w in WORKLOADS}
+# A smaller member of the causal GQA-sink family (inputs still larger than L2),
+# used for detailed hardware-counter captures.
+PROFILE_WORKLOADS = [
+    Workload("gqa_sink_causal_s16384_h16", "bf16", B=1, Hq=16, Hkv=2, Sq=16384, Skv=16384,
+             mask_kind=MASK_CAUSAL, sink=True, seed=5),
+]
+BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_WORKLOADS}
 
 
 @dataclass
