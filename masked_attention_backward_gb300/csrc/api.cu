@@ -17,7 +17,7 @@
 
 #include <mutex>
 
-#include "../../include/maskattn.h"
+#include "maskattn.h"
 #include "internal.h"
 #include "tmap.h"
 

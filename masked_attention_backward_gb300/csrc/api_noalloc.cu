@@ -20,7 +20,7 @@
 // threads without ordering) race on the array and give wrong results.
 #include <mutex>
 
-#include "../../include/maskattn.h"
+#include "maskattn.h"
 #include "internal.h"
 
 namespace {
