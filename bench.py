@@ -42,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # Files whose content decides the dK/dV and dQ kernels' DRAM traffic.
 KERNEL_SOURCES = {
     "k_dkdv": ["csrc/attn_kv.cu", "csrc/tiles.cuh", "csrc/ptx.cuh", "csrc/internal.h"],
-    "k_dq": ["csrc/attn_q.cu", "csrc/tiles.cuh", "csrc/ptx.cuh", "csrc/internal.h"],
+    "k_dq": ["csrc/attn_dq.cu", "csrc/tiles.cuh", "csrc/ptx.cuh", "csrc/internal.h"],
 }
 
 

@@ -10,7 +10,7 @@
 //   k_mask_transpose +  block masks only: transposed mask and both
 //   k_build_sel           select tables
 //   k_dkdv              key-stationary dK / dV
-//   k_qside<dQ>         query-stationary dQ
+//   k_dq                query-stationary dQ
 //   k_dsink_finalize    sink only: dSink = -sum of partials
 #include <stdlib.h>
 #include <string.h>

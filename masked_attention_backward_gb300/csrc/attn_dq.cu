@@ -1,0 +1,330 @@
+// attn_dq.cu -- query-stationary dQ kernel on tcgen05 / TMEM, fed by TMA.
+//
+// One CTA per (b, query head h, Q_TILE query rows).  Q and dO of the tile are
+// loaded once and copied into TMEM, where they serve as the A operand of
+// every score contraction.  For each active key sub-tile t of Q_SUB rows:
+//   S  = Q K_t^T,  dP = dO V_t^T                 (A from TMEM, fp32 in TMEM)
+//   P  = exp2(S * scale*log2e - lse2),  dS = P (dP - Delta)   (softmax warps)
+//   dQ += dS K_t                                  (A = dS from TMEM)
+// then dQ *= scale, rounded to the input dtype and written once.
+//
+// Sources: tilelang-ascend PR #1 "Add GQA Sink Backward BHSD", commit notes
+// (five contractions + softmax + dS per KV step; P recomputed from LSE);
+// cannbot-knowledge PR #174, BlockSparseAttentionGrad runbook, skeleton
+// "delta -> dq -> dkdv" with dq walking the query-major select table, and the
+// precision notes (p = exp(s - lse), ds = p (dp - delta), fp16 / bf16
+// operands into the contraction with fp32 accumulation).
+//
+// Why the operands sit where they do: an MMA whose A and B both come from
+// shared memory at N = 64 is limited by shared-memory bandwidth (it reads
+// 6 KB per 32 cycles of math), while with A in TMEM it reads only its 2 KB B
+// tile and runs at the tensor pipe's rate.  Q and dO are the same for the
+// whole walk, so they move to TMEM once.
+//
+// TMEM columns (512): dQ accumulator [0,128), Q [128,192), dO [192,256)
+// (16-bit pairs), and two S/dP buffers of 128 columns at 256 and 384 (S in
+// the first 64, dP in the next 64; dS is packed over the start of S).
+//
+// MMA order: dQ(n), then dP(n+2) into the dP half of the buffer dQ(n) is not
+// reading, then -- once dQ(n) has completed -- S(n+2) over dS(n).  The wait
+// for dQ(n) is covered by dP(n+2) already queued behind it, so the tensor
+// pipe never drains between steps.
+//
+// Warp roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs (whole warp, one elected lane), warps 2..9 are two groups
+// of four warps; warp (sp, g) owns TMEM lanes 32 sp .. 32 sp + 31 and key
+// columns 32 g .. 32 g + 31 of each sub-tile.
+#include <math.h>
+
+#include "tiles.cuh"
+
+namespace mab {
+
+namespace dq_side {
+
+constexpr int STAGES = 4;     // K/V ring depth
+constexpr int COL_ACC = 0;    // dQ accumulator, 128 fp32 columns
+constexpr int COL_QA = 128;   // Q as the A operand, 64 columns of 16-bit pairs
+constexpr int COL_DOA = 192;  // dO as the A operand
+constexpr int COL_BUF = 256;  // buffer b: S at COL_BUF + 128 b, dP at +64
+constexpr int NUM_THREADS = 320;
+
+struct __align__(1024) Smem {
+  uint8_t Q[2 * Q_TILE * 128];  // two 64-column chunks, 128B swizzle
+  uint8_t dO[2 * Q_TILE * 128];
+  uint8_t K[STAGES][2 * Q_SUB * 128];
+  uint8_t V[STAGES][2 * Q_SUB * 128];
+  uint64_t bar_q_full;          // Q, dO landed in shared memory
+  uint64_t bar_qa_full;         // Q, dO copied into TMEM (8 softmax warps)
+  uint64_t bar_kv_full[STAGES];
+  uint64_t bar_kv_empty[STAGES];
+  uint64_t bar_s_full[2];       // S and dP of the buffer complete
+  uint64_t bar_p_full[2];       // dS of the buffer packed (8 softmax warps)
+  uint64_t bar_acc_free[2];     // dQ MMA that read the buffer's dS complete
+  uint64_t bar_acc_full;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
+
+enum { TAG_Q = 0x301, TAG_QA, TAG_KV_EMPTY, TAG_KV_FULL, TAG_P_FULL, TAG_S_FULL, TAG_ACC_FREE,
+       TAG_ACC };
+
+}  // namespace dq_side
+
+template <bool BF16>
+__global__ void __launch_bounds__(dq_side::NUM_THREADS, 1)
+k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tdO,
+     const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
+     uint16_t* __restrict__ dq, const AttnParams p) {
+  using namespace dq_side;
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int BH = p.B * p.Hq;
+  const int qt = p.nQT_q - 1 - (int)(blockIdx.x / BH);  // longest causal rows first
+  const int bh = (int)(blockIdx.x % BH);
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int kvh = b * p.Hkv + h / p.group;
+  const int q0 = qt * Q_TILE;
+  QWalk walk;
+  walk.init(p, bh, qt);
+  const int N = walk.cnt;
+  WaitCtx wc{p.status, &s.abort_flag, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    s.abort_flag = 0;
+    mbar_init(smem_u32(&s.bar_q_full), 1);
+    mbar_init(smem_u32(&s.bar_qa_full), 8);
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(smem_u32(&s.bar_kv_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_kv_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.bar_s_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_p_full[i]), 8);
+      mbar_init(smem_u32(&s.bar_acc_free[i]), 1);
+    }
+    mbar_init(smem_u32(&s.bar_acc_full), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = s.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tQ);
+      tma_prefetch_desc(&tdO);
+      tma_prefetch_desc(&tK);
+      tma_prefetch_desc(&tV);
+      const uint32_t qbar = smem_u32(&s.bar_q_full);
+      mbar_arrive_expect_tx(qbar, 4 * Q_TILE * 128);
+      tma_load_3d(smem_u32(s.Q), &tQ, 0, q0, bh, qbar);
+      tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, q0, bh, qbar);
+      tma_load_3d(smem_u32(s.dO), &tdO, 0, q0, bh, qbar);
+      tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, q0, bh, qbar);
+      for (int n = 0; n < N; ++n) {
+        const int st = n % STAGES;
+        if (n >= STAGES &&
+            !mbar_wait(smem_u32(&s.bar_kv_empty[st]), ((n / STAGES) - 1) & 1, wc, TAG_KV_EMPTY))
+          break;
+        const int t = walk.tile(n);
+        const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
+        mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
+        tma_load_3d(smem_u32(s.K[st]), &tK, 0, t * Q_SUB, kvh, fb);
+        tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, t * Q_SUB, kvh, fb);
+        tma_load_3d(smem_u32(s.V[st]), &tV, 0, t * Q_SUB, kvh, fb);
+        tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, t * Q_SUB, kvh, fb);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (whole warp)
+    constexpr uint32_t ID_S = idesc_f16(BF16, Q_TILE, Q_SUB, false, false);
+    constexpr uint32_t ID_ACC = idesc_f16(BF16, Q_TILE, HEAD_DIM, false, true);
+    // S(m) = Q K^T into buffer m & 1 (A = Q from TMEM, B = K tile, K-major)
+    auto issue_s = [&](int m) {
+      const uint32_t d = tbase + COL_BUF + (m & 1) * 128;
+      const uint64_t bK = sdesc_sw128(smem_u32(s.K[m % STAGES]), 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+        mma_ts_w(d, tbase + COL_QA + 8 * kk,
+                 bK + (uint64_t)(((kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                 kk > 0 ? 1u : 0u);
+    };
+    // dP(m) = dO V^T into the dP half of buffer m & 1
+    auto issue_dp = [&](int m) {
+      const uint32_t d = tbase + COL_BUF + (m & 1) * 128 + 64;
+      const uint64_t bV = sdesc_sw128(smem_u32(s.V[m % STAGES]), 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+        mma_ts_w(d, tbase + COL_DOA + 8 * kk,
+                 bV + (uint64_t)(((kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                 kk > 0 ? 1u : 0u);
+    };
+    // dQ += dS(m) K (A = dS packed in buffer m & 1, B = K tile, MN-major)
+    auto issue_dq = [&](int m) {
+      const uint32_t a = tbase + COL_BUF + (m & 1) * 128;
+      const uint64_t bK = sdesc_sw128(smem_u32(s.K[m % STAGES]), Q_SUB * 128, 1024);
+#pragma unroll
+      for (int kk = 0; kk < Q_SUB / 16; ++kk)
+        mma_ts_w(tbase + COL_ACC, a + 32 * (kk >> 1) + 8 * (kk & 1),
+                 bK + (uint64_t)((kk * 2048) >> 4), ID_ACC, (m > 0 || kk > 0) ? 1u : 0u);
+    };
+    bool ok = N == 0 || mbar_wait_warp(smem_u32(&s.bar_qa_full), 0, wc, TAG_QA);
+    tc_fence_after();
+    for (int m = 0; ok && m < N && m < 2; ++m) {
+      ok = mbar_wait_warp(smem_u32(&s.bar_kv_full[m % STAGES]), (m / STAGES) & 1, wc, TAG_KV_FULL);
+      if (!ok) break;
+      tc_fence_after();
+      issue_s(m);
+      issue_dp(m);
+      mma_commit_w(smem_u32(&s.bar_s_full[m & 1]));
+    }
+    for (int n = 0; ok && n < N; ++n) {
+      const int bf = n & 1;
+      ok = mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), (n >> 1) & 1, wc, TAG_P_FULL);
+      if (!ok) break;
+      tc_fence_after();
+      issue_dq(n);
+      mma_commit_w(smem_u32(&s.bar_kv_empty[n % STAGES]));
+      mma_commit_w(smem_u32(&s.bar_acc_free[bf]));
+      const int m = n + 2;
+      if (m < N) {
+        ok = mbar_wait_warp(smem_u32(&s.bar_kv_full[m % STAGES]), (m / STAGES) & 1, wc,
+                            TAG_KV_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        issue_dp(m);  // the dP half was last read by the softmax warps of step n
+        ok = mbar_wait_warp(smem_u32(&s.bar_acc_free[bf]), (n >> 1) & 1, wc, TAG_ACC_FREE);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(m);  // overwrites dS(n), which dQ(n) has finished reading
+        mma_commit_w(smem_u32(&s.bar_s_full[bf]));
+      }
+    }
+    // completes when every MMA issued above has (also on the abort path, so
+    // that TMEM is idle before it is freed)
+    mma_commit_w(smem_u32(&s.bar_acc_full));
+    mbar_wait_warp(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int sp = warp & 3, g = (warp - 2) >> 2;
+    const int rloc = sp * 32 + lane;
+    const int i = q0 + rloc;
+    const uint32_t lane_base = tbase + ((uint32_t)(sp * 32) << 16);
+    bool ok = mbar_wait(smem_u32(&s.bar_q_full), 0, wc, TAG_Q);
+    if (ok) {
+      // Q and dO rows into TMEM as 16-bit pairs (element 2c in the low half
+      // of column c): this warp copies d columns 64 g .. 64 g + 63 of its rows.
+      const uint8_t* src[2] = {s.Q + g * (Q_TILE * 128) + rloc * 128,
+                               s.dO + g * (Q_TILE * 128) + rloc * 128};
+      const uint32_t dst[2] = {COL_QA + 32u * g, COL_DOA + 32u * g};
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src[which] + ((c ^ (rloc & 7)) << 4));
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
+        }
+        tmem_st32(lane_base + dst[which], w);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.bar_qa_full));
+
+    const size_t srow = (size_t)bh * p.Sq_pad + i;
+    const float lse2_i = p.lse2[srow];
+    const float delta_i = p.delta[srow];
+    for (int n = 0; ok && n < N; ++n) {
+      const int bf = n & 1;
+      if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (n >> 1) & 1, wc, TAG_S_FULL)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int t = walk.tile(n);
+      const uint32_t vis = vis_query_row(p, bh, i, t * Q_SUB + 32 * g);
+      const uint32_t col = COL_BUF + bf * 128 + 32 * g;
+      float sv[32], dp[32];
+      tmem_ld32(lane_base + col, sv);
+      tmem_ld32(lane_base + col + 64, dp);
+      tmem_wait_ld();
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -lse2_i));
+        float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -lse2_i));
+        p0 = ((vis >> (2 * c)) & 1u) ? p0 : 0.f;
+        p1 = ((vis >> (2 * c + 1)) & 1u) ? p1 : 0.f;
+        pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
+      }
+      tmem_st16(lane_base + col, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s.bar_p_full[bf]));
+    }
+    // ---------------------------------------------------------- epilogue
+    // Columns [64 g, 64 g + 64) of the accumulator, one row per lane.
+    uint32_t pk[32];
+    bool have = ok && N > 0;
+    if (have) have = mbar_wait(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
+    tc_fence_after();
+    if (have) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float v[32];
+        tmem_ld32(lane_base + COL_ACC + 64 * g + 32 * half, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          pk[16 * half + c] = pack2<BF16>(v[2 * c] * p.scale, v[2 * c + 1] * p.scale);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) pk[c] = 0u;
+    }
+    // The Q tile in shared memory is dead once it is in TMEM (every softmax
+    // warp passed its copy before reaching here); it stages the output rows.
+    named_bar_sync(1, 256);
+    uint8_t* stage = s.Q + (warp - 2) * 4096;
+    const int r0 = q0 + sp * 32;
+    uint16_t* orow = dq + ((size_t)bh * p.Sq + r0) * HEAD_DIM + 64 * g;
+    warp_store_rows(stage, pk, orow, min(32, p.Sq - r0));
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+cudaError_t launch_dq(bool bf16, const AttnParams& p, const CUtensorMap& tQ, const CUtensorMap& tdO,
+                      const CUtensorMap& tK, const CUtensorMap& tV, void* dq, cudaStream_t st) {
+  auto kern = bf16 ? k_dq<true> : k_dq<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)dq_side::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)(p.nQT_q * p.B * p.Hq));
+  kern<<<grid, dq_side::NUM_THREADS, dq_side::SMEM_BYTES, st>>>(tQ, tdO, tK, tV, (uint16_t*)dq,
+                                                                 p);
+  return cudaGetLastError();
+}
+
+}  // namespace mab

@@ -1,22 +1,17 @@
-// attn_q.cu -- query-stationary kernels on tcgen05 / TMEM, fed by TMA.
+// attn_fwd.cu -- forward kernel producing O and LSE (the inputs of the
+// backward), query-stationary on tcgen05 / TMEM, fed by TMA.
 //
-//   k_qside<BF16, false>  (dQ): one CTA per (b, q-head, Q_TILE query rows).
-//     For every active key sub-tile t (Q_SUB rows):
-//       S  = Q K_t^T,  dP = dO V_t^T                (SS MMA, fp32 in TMEM)
-//       P  = exp2(S * scale*log2e - lse2),  dS = P (dP - Delta)   (softmax warps)
-//       dQ += dS K_t                                 (TS MMA, dS from TMEM)
-//     then dQ *= scale, rounded to the input dtype, written once.
-//   k_qside<BF16, true>   (forward, two passes over the same key tiles):
-//     pass A: S = Q K_t^T, running max / sum per row, seeded with the sink;
-//     pass B: S again, P = exp2(S*c - lse2) exactly, O += P V_t.
-//     No rescaling of O is ever needed because pass B knows the final lse.
+// One CTA per (b, query head, Q_TILE query rows); two passes over the same
+// active key sub-tiles t (Q_SUB rows):
+//   pass A: S = Q K_t^T, running max / sum per row in the log2 domain,
+//           seeded with the sink logit (which joins only the denominator);
+//   pass B: S again, P = exp2(S * scale*log2e - lse2) exactly, O += P V_t.
+// No rescaling of O is ever needed because pass B knows the final LSE.
 //
-// Sources: tilelang-ascend PR #1 "Add GQA Sink Backward BHSD", commit notes
-// (five contractions + softmax + dS per KV step; online softmax with sink and
-// window in the forward); cannbot-knowledge PR #174, BlockSparseAttentionGrad
-// runbook, skeleton "delta -> dq -> dkdv" with dq walking the query-major
-// select table, precision notes (p = exp(s - lse), ds = p (dp - delta), fp16
-// / bf16 operands into the contraction with fp32 accumulation).
+// Sources: tilelang-ascend PR #1 "Add GQA Sink Backward BHSD", Summary
+// (online softmax with an attention sink and a sliding window);
+// cannbot-knowledge PR #174, BlockSparseAttentionGrad runbook, precision
+// notes (a row that sees no key gets zeros).
 //
 // Warp roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
 // issues the MMAs (one thread), warps 2..9 are two groups of four warps that
@@ -27,20 +22,19 @@
 
 namespace mab {
 
-namespace q_side {
+namespace fwd_side {
 
 constexpr int STAGES = 3;   // K/V ring depth
 constexpr int NBUF = 3;     // S/dP buffers in TMEM
-constexpr int COL_ACC = 0;  // dQ or O accumulator: 128 fp32 columns
-constexpr int COL_S = 128;  // buffer b: S at COL_S + 128 b, dP at +64
+constexpr int COL_ACC = 0;  // O accumulator: 128 fp32 columns
+constexpr int COL_S = 128;  // buffer b: S at COL_S + 128 b
 constexpr int NUM_THREADS = 320;
 
 struct __align__(1024) Smem {
   uint8_t Q[2 * Q_TILE * 128];          // two 64-column chunks, 128B swizzle
-  uint8_t dO[2 * Q_TILE * 128];
   uint8_t K[STAGES][2 * Q_SUB * 128];
   uint8_t V[STAGES][2 * Q_SUB * 128];
-  float ml[2][Q_TILE][2];               // forward: per-group (max, sum) per row
+  float ml[2][Q_TILE][2];               // per-group (max, sum) per row
   uint64_t bar_q_full;
   uint64_t bar_kv_full[STAGES];
   uint64_t bar_kv_empty[STAGES];
@@ -60,14 +54,14 @@ constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
 enum { TAG_Q = 0x101, TAG_KV_EMPTY, TAG_KV_FULL, TAG_S_FREE, TAG_P_FULL, TAG_S_FULL, TAG_ACC,
        TAG_ML, TAG_DRAIN };
 
-}  // namespace q_side
+}  // namespace fwd_side
 
-template <bool BF16, bool FWD>
-__global__ void __launch_bounds__(q_side::NUM_THREADS, 1)
-k_qside(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tdO,
-        const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
-        uint16_t* __restrict__ out, const AttnParams p) {
-  using namespace q_side;
+template <bool BF16>
+__global__ void __launch_bounds__(fwd_side::NUM_THREADS, 1)
+k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tK,
+           const __grid_constant__ CUtensorMap tV, uint16_t* __restrict__ out,
+           const AttnParams p) {
+  using namespace fwd_side;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -81,7 +75,7 @@ k_qside(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
   QWalk walk;
   walk.init(p, bh, qt);
   const int N = walk.cnt;
-  const int NT = FWD ? 2 * N : N;
+  const int NT = 2 * N;  // pass A, then pass B
   WaitCtx wc{p.status, &s.abort_flag, p.timeout_ns};
 
   if (threadIdx.x == 0) {
@@ -116,22 +110,17 @@ k_qside(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
       tma_prefetch_desc(&tQ);
       tma_prefetch_desc(&tK);
       tma_prefetch_desc(&tV);
-      if (!FWD) tma_prefetch_desc(&tdO);
       const uint32_t qbar = smem_u32(&s.bar_q_full);
-      mbar_arrive_expect_tx(qbar, FWD ? 2 * Q_TILE * 128 : 4 * Q_TILE * 128);
+      mbar_arrive_expect_tx(qbar, 2 * Q_TILE * 128);
       tma_load_3d(smem_u32(s.Q), &tQ, 0, q0, bh, qbar);
       tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, q0, bh, qbar);
-      if (!FWD) {
-        tma_load_3d(smem_u32(s.dO), &tdO, 0, q0, bh, qbar);
-        tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, q0, bh, qbar);
-      }
       for (int n = 0; n < NT; ++n) {
         const int st = n % STAGES;
         if (n >= STAGES &&
             !mbar_wait(smem_u32(&s.bar_kv_empty[st]), ((n / STAGES) - 1) & 1, wc, TAG_KV_EMPTY))
           break;
-        const int t = walk.tile(FWD && n >= N ? n - N : n);
-        const bool loadV = !FWD || n >= N;
+        const int t = walk.tile(n >= N ? n - N : n);
+        const bool loadV = n >= N;  // pass A needs K only
         const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
         mbar_arrive_expect_tx(fb, loadV ? 4 * Q_SUB * 128 : 2 * Q_SUB * 128);
         tma_load_3d(smem_u32(s.K[st]), &tK, 0, t * Q_SUB, kvh, fb);
@@ -147,20 +136,19 @@ k_qside(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
     if (lane == 0) {
       constexpr uint32_t ID_S = idesc_f16(BF16, Q_TILE, Q_SUB, false, false);
       constexpr uint32_t ID_ACC = idesc_f16(BF16, Q_TILE, HEAD_DIM, false, true);
-      const uint32_t sQ = smem_u32(s.Q), sdO = smem_u32(s.dO);
+      const uint32_t sQ = smem_u32(s.Q);
       auto consume = [&](int m) -> bool {
         const int bf = m % NBUF, st = m % STAGES;
         if (!mbar_wait(smem_u32(&s.bar_p_full[bf]), (m / NBUF) & 1, wc, TAG_P_FULL)) return false;
         tc_fence_after();
-        if (!FWD || m >= N) {
-          const int first = FWD ? N : 0;
+        if (m >= N) {  // pass B: O += P V
           const uint32_t colS = tbase + COL_S + bf * 128;
-          const uint32_t bop = smem_u32(FWD ? s.V[st] : s.K[st]);
+          const uint32_t bop = smem_u32(s.V[st]);
 #pragma unroll
           for (int kk = 0; kk < Q_SUB / 16; ++kk) {
             const uint32_t a_tmem = colS + 32 * (kk >> 1) + 8 * (kk & 1);
             mma_ts(tbase + COL_ACC, a_tmem, sdesc_sw128(bop + kk * 2048, Q_SUB * 128, 1024), ID_ACC,
-                   (m > first || kk > 0) ? 1u : 0u);
+                   (m > N || kk > 0) ? 1u : 0u);
           }
         }
         mma_commit(smem_u32(&s.bar_kv_empty[st]));
@@ -190,15 +178,6 @@ k_qside(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
           mma_ss(colS, sdesc_sw128(sQ + ao, 16, 1024), sdesc_sw128(sK + bo, 16, 1024), ID_S,
                  kk > 0 ? 1u : 0u);
         }
-        if (!FWD) {
-#pragma unroll
-          for (int kk = 0; kk < HEAD_DIM / 16; ++kk) {
-            const uint32_t ao = (kk >> 2) * (Q_TILE * 128) + (kk & 3) * 32;
-            const uint32_t bo = (kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32;
-            mma_ss(colS + 64, sdesc_sw128(sdO + ao, 16, 1024), sdesc_sw128(sV + bo, 16, 1024),
-                   ID_S, kk > 0 ? 1u : 0u);
-          }
-        }
         mma_commit(smem_u32(&s.bar_s_full[bf]));
         if (n >= 1 && !consume(n - 1)) {
           ok = false;
@@ -216,42 +195,9 @@ k_qside(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
     const int rloc = sp * 32 + lane;
     const int i = q0 + rloc;
     const uint32_t lane_base = tbase + ((uint32_t)(sp * 32) << 16);
-    const size_t srow = (size_t)bh * p.Sq_pad + i;
-    float lse2_i = 0.f, delta_i = 0.f;
+    float lse2_i = 0.f;
     bool ok = true;
-    if (!FWD) {
-      lse2_i = p.lse2[srow];
-      delta_i = p.delta[srow];
-      for (int n = 0; n < N; ++n) {
-        const int bf = n % NBUF;
-        if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (n / NBUF) & 1, wc, TAG_S_FULL)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int t = walk.tile(n);
-        const uint32_t vis = vis_query_row(p, bh, i, t * Q_SUB + 32 * g);
-        const uint32_t col = COL_S + bf * 128 + 32 * g;
-        float sv[32], dp[32];
-        tmem_ld32(lane_base + col, sv);
-        tmem_ld32(lane_base + col + 64, dp);
-        tmem_wait_ld();
-        uint32_t pk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -lse2_i));
-          float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -lse2_i));
-          p0 = ((vis >> (2 * c)) & 1u) ? p0 : 0.f;
-          p1 = ((vis >> (2 * c + 1)) & 1u) ? p1 : 0.f;
-          pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
-        }
-        tmem_st16(lane_base + col, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&s.bar_p_full[bf]));
-      }
-    } else {
+    {
       // pass A: running max / sum in the log2 domain
       float m_run = -INFINITY, l_run = 0.f;
       if (g == 0 && p.sink) {
@@ -338,14 +284,13 @@ k_qside(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
     if (have) have = mbar_wait(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
     tc_fence_after();
     if (have) {
-      const float osc = FWD ? 1.f : p.scale;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float v[32];
         tmem_ld32(lane_base + COL_ACC + 64 * g + 32 * half, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[16 * half + c] = pack2<BF16>(v[2 * c] * osc, v[2 * c + 1] * osc);
+        for (int c = 0; c < 16; ++c) pk[16 * half + c] = pack2<BF16>(v[2 * c], v[2 * c + 1]);
       }
     } else {
 #pragma unroll
@@ -368,27 +313,15 @@ k_qside(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
   }
 }
 
-template <bool FWD>
-static cudaError_t launch_qside(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
-                                const CUtensorMap& tdO, const CUtensorMap& tK,
-                                const CUtensorMap& tV, void* out, cudaStream_t st) {
-  auto kern = bf16 ? k_qside<true, FWD> : k_qside<false, FWD>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)q_side::SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(p.nQT_q * p.B * p.Hq));
-  kern<<<grid, q_side::NUM_THREADS, q_side::SMEM_BYTES, st>>>(tQ, tdO, tK, tV, (uint16_t*)out, p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dq(bool bf16, const AttnParams& p, const CUtensorMap& tQ, const CUtensorMap& tdO,
-                      const CUtensorMap& tK, const CUtensorMap& tV, void* dq, cudaStream_t st) {
-  return launch_qside<false>(bf16, p, tQ, tdO, tK, tV, dq, st);
-}
-
 cudaError_t launch_fwd(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                        const CUtensorMap& tK, const CUtensorMap& tV, void* o, cudaStream_t st) {
-  return launch_qside<true>(bf16, p, tQ, tQ, tK, tV, o, st);
+  auto kern = bf16 ? k_attn_fwd<true> : k_attn_fwd<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)fwd_side::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)(p.nQT_q * p.B * p.Hq));
+  kern<<<grid, fwd_side::NUM_THREADS, fwd_side::SMEM_BYTES, st>>>(tQ, tK, tV, (uint16_t*)o, p);
+  return cudaGetLastError();
 }
 
 }  // namespace mab
