@@ -1,12 +1,14 @@
 // attn_kv.cu -- key-stationary dK/dV kernel on tcgen05 / TMEM, fed by TMA.
 //
 // One CTA per (b, kv head c, KV_TILE key rows).  K and V of the tile are
-// loaded once.  The CTA walks every query head of the GQA group and, for each,
-// every active query sub-tile r of KV_SUB rows (closed-form range for causal /
-// sliding / none, the key-major select table for block masks):
-//   S^T  = K Q_r^T,   dP^T = V dO_r^T                (SS MMA, fp32 in TMEM)
+// loaded once; K is copied into TMEM.  The CTA walks every query head of the
+// GQA group and, for each, every active query sub-tile r of KV_SUB rows
+// (closed-form range for causal / sliding / none, the key-major select table
+// for block masks):
+//   S^T  = K Q_r^T            (A = K from TMEM)
+//   dP^T = V dO_r^T           (A = V from shared memory)
 //   P^T  = exp2(S^T * scale*log2e - lse2_r),  dS^T = P^T (dP^T - Delta_r)
-//   dV  += P^T dO_r,  dK += dS^T Q_r                 (TS MMA, P^T / dS^T from TMEM)
+//   dV  += P^T dO_r,  dK += dS^T Q_r          (A = P^T / dS^T from TMEM)
 // The group reduction happens in the TMEM accumulators; the epilogue scales
 // dK, rounds both to the input dtype and writes each row once, contiguously.
 //
@@ -20,6 +22,24 @@
 // Computing S^T rather than S puts key rows on the TMEM lanes, which is the
 // row layout the A operand of dV += P^T dO and dK += dS^T Q needs, so P^T and
 // dS^T go back into TMEM and never touch shared memory.
+//
+// TMEM columns (512): dV [0,128), dK [128,256), K as 16-bit pairs [256,320),
+// two S^T buffers [320,384) and [384,448), dP^T [448,512).  Softmax group g
+// owns query columns 32 g .. 32 g + 31 of a sub-tile, i.e. 32 fp32 columns of
+// an S^T buffer; it packs P^T into the first 16 of them and dS^T into the
+// last 16.  dS^T therefore does not occupy the dP^T buffer, which is free
+// again as soon as the softmax warps have read it.
+//
+// MMA order per step n: dV(n), dK(n), dP(n+1), S(n+2).  S(n+2) overwrites the
+// buffer that dV(n) / dK(n) read, and its wait for them is covered by dP(n+1)
+// queued behind; dP(n+1) waits only on the softmax warps having read dP(n).
+// Between dP(n+1) completing and dK(n+1) being needed lie S(n+2) and dV(n+1),
+// and between S(n+2) completing and dV(n+2) lie three more groups, so the
+// softmax work of a step is hidden behind the tensor pipe.
+//
+// Warp roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues the MMAs (whole warp, one elected lane), warps 2..9 are the softmax
+// warps: warp (sp, g) owns TMEM lanes 32 sp .. 32 sp + 31 (key rows).
 #include <math.h>
 
 #include "tiles.cuh"
@@ -28,36 +48,39 @@ namespace mab {
 
 namespace kv_side {
 
-constexpr int STAGES = 3;   // Q/dO ring depth
-constexpr int NBUF = 2;     // S/dP buffers in TMEM
+constexpr int STAGES = 4;      // Q/dO ring depth
 constexpr int COL_DV = 0;
 constexpr int COL_DK = 128;
-constexpr int COL_S = 256;  // buffer b: S^T at COL_S + 128 b, dP^T at +64
+constexpr int COL_KA = 256;    // K as the A operand (64 columns of 16-bit pairs)
+constexpr int COL_ST = 320;    // S^T buffer b at COL_ST + 64 b
+constexpr int COL_DPT = 448;   // dP^T
 constexpr int NUM_THREADS = 320;
 
 struct __align__(1024) Smem {
-  uint8_t K[2 * KV_TILE * 128];
+  uint8_t K[2 * KV_TILE * 128];  // dead once copied into TMEM: stages the output
   uint8_t V[2 * KV_TILE * 128];
   uint8_t Q[STAGES][2 * KV_SUB * 128];
   uint8_t dO[STAGES][2 * KV_SUB * 128];
   float lse2[STAGES][KV_SUB];
   float delta[STAGES][KV_SUB];
-  uint64_t bar_kv_full;
+  uint64_t bar_kv_full;          // K, V landed
+  uint64_t bar_ka_full;          // K copied into TMEM (8 softmax warps)
   uint64_t bar_q_full[STAGES];
   uint64_t bar_q_empty[STAGES];
-  uint64_t bar_s_full[NBUF];
-  uint64_t bar_p_full[NBUF];
-  uint64_t bar_s_free[NBUF];
+  uint64_t bar_s_full[2];        // S^T of the buffer complete
+  uint64_t bar_p_full[2];        // P^T of the buffer packed (8 warps)
+  uint64_t bar_st_free[2];       // dV / dK MMAs that read the buffer complete
+  uint64_t bar_dp_full;          // dP^T complete
+  uint64_t bar_ds_full;          // dS^T packed, dP^T read (8 warps)
   uint64_t bar_acc_full;
-  uint64_t bar_drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
 
-enum { TAG_KV = 0x201, TAG_Q_EMPTY, TAG_Q_FULL, TAG_S_FREE, TAG_P_FULL, TAG_S_FULL, TAG_ACC,
-       TAG_DRAIN };
+enum { TAG_KV = 0x201, TAG_KA, TAG_Q_EMPTY, TAG_Q_FULL, TAG_ST_FREE, TAG_P_FULL, TAG_S_FULL,
+       TAG_DP_FULL, TAG_DS_FULL, TAG_ACC };
 
 }  // namespace kv_side
 
@@ -84,17 +107,19 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
     mbar_init(smem_u32(&s.bar_kv_full), 1);
+    mbar_init(smem_u32(&s.bar_ka_full), 8);
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_u32(&s.bar_q_full[i]), 1);
       mbar_init(smem_u32(&s.bar_q_empty[i]), 1);
     }
-    for (int i = 0; i < NBUF; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_s_full[i]), 1);
       mbar_init(smem_u32(&s.bar_p_full[i]), 8);
-      mbar_init(smem_u32(&s.bar_s_free[i]), 1);
+      mbar_init(smem_u32(&s.bar_st_free[i]), 1);
     }
+    mbar_init(smem_u32(&s.bar_dp_full), 1);
+    mbar_init(smem_u32(&s.bar_ds_full), 8);
     mbar_init(smem_u32(&s.bar_acc_full), 1);
-    mbar_init(smem_u32(&s.bar_drain), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -141,88 +166,129 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t ID_S = idesc_f16(BF16, KV_TILE, KV_SUB, false, false);
-      constexpr uint32_t ID_ACC = idesc_f16(BF16, KV_TILE, HEAD_DIM, false, true);
-      const uint32_t sK = smem_u32(s.K), sV = smem_u32(s.V);
-      auto consume = [&](int m) -> bool {
-        const int bf = m % NBUF, st = m % STAGES;
-        if (!mbar_wait(smem_u32(&s.bar_p_full[bf]), (m / NBUF) & 1, wc, TAG_P_FULL)) return false;
-        tc_fence_after();
-        const uint32_t colS = tbase + COL_S + bf * 128;
-        const uint32_t sQ = smem_u32(s.Q[st]), sdO = smem_u32(s.dO[st]);
+    // ------------------------------------------------------------ MMA issuer (whole warp)
+    constexpr uint32_t ID_S = idesc_f16(BF16, KV_TILE, KV_SUB, false, false);
+    constexpr uint32_t ID_ACC = idesc_f16(BF16, KV_TILE, HEAD_DIM, false, true);
+    // S^T(m) = K Q^T into buffer m & 1 (A = K from TMEM, B = Q tile, K-major)
+    auto issue_s = [&](int m) {
+      const uint32_t d = tbase + COL_ST + 64 * (m & 1);
+      const uint64_t bQ = sdesc_sw128(smem_u32(s.Q[m % STAGES]), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < KV_SUB / 16; ++kk) {
-          const uint32_t a_off = 32 * (kk >> 1) + 8 * (kk & 1);
-          mma_ts(tbase + COL_DV, colS + a_off, sdesc_sw128(sdO + kk * 2048, KV_SUB * 128, 1024),
-                 ID_ACC, (m > 0 || kk > 0) ? 1u : 0u);
-        }
+      for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+        mma_ts_w(d, tbase + COL_KA + 8 * kk,
+                 bQ + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                 kk > 0 ? 1u : 0u);
+    };
+    // dP^T(m) = V dO^T (A = V tile, B = dO tile, both K-major in shared memory)
+    auto issue_dp = [&](int m) {
+      const uint64_t aV = sdesc_sw128(smem_u32(s.V), 16, 1024);
+      const uint64_t bO = sdesc_sw128(smem_u32(s.dO[m % STAGES]), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < KV_SUB / 16; ++kk) {
-          const uint32_t a_off = 32 * (kk >> 1) + 8 * (kk & 1);
-          mma_ts(tbase + COL_DK, colS + 64 + a_off, sdesc_sw128(sQ + kk * 2048, KV_SUB * 128, 1024),
-                 ID_ACC, (m > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&s.bar_q_empty[st]));
-        mma_commit(smem_u32(&s.bar_s_free[bf]));
-        return true;
-      };
-      bool ok = mbar_wait(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV);
+      for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+        mma_ss_w(tbase + COL_DPT,
+                 aV + (uint64_t)(((kk >> 2) * (KV_TILE * 128) + (kk & 3) * 32) >> 4),
+                 bO + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                 kk > 0 ? 1u : 0u);
+    };
+    // dV += P^T(m) dO, dK += dS^T(m) Q (A from buffer m & 1, B MN-major)
+    auto issue_acc = [&](int m, bool dkside) {
+      const uint32_t a = tbase + COL_ST + 64 * (m & 1) + (dkside ? 16 : 0);
+      const uint64_t bB = sdesc_sw128(smem_u32(dkside ? s.Q[m % STAGES] : s.dO[m % STAGES]),
+                                      KV_SUB * 128, 1024);
+#pragma unroll
+      for (int kk = 0; kk < KV_SUB / 16; ++kk)
+        mma_ts_w(tbase + (dkside ? COL_DK : COL_DV), a + 32 * (kk >> 1) + 8 * (kk & 1),
+                 bB + (uint64_t)((kk * 2048) >> 4), ID_ACC, (m > 0 || kk > 0) ? 1u : 0u);
+    };
+    bool ok = true;
+    if (N > 0) {
+      ok = mbar_wait_warp(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV) &&
+           mbar_wait_warp(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA) &&
+           mbar_wait_warp(smem_u32(&s.bar_q_full[0]), 0, wc, TAG_Q_FULL);
       tc_fence_after();
-      for (int n = 0; ok && n < N; ++n) {
-        const int st = n % STAGES, bf = n % NBUF;
-        if (!mbar_wait(smem_u32(&s.bar_q_full[st]), (n / STAGES) & 1, wc, TAG_Q_FULL)) {
-          ok = false;
-          break;
-        }
-        if (n >= NBUF &&
-            !mbar_wait(smem_u32(&s.bar_s_free[bf]), ((n / NBUF) - 1) & 1, wc, TAG_S_FREE)) {
-          ok = false;
-          break;
-        }
+      if (ok) {
+        issue_s(0);
+        mma_commit_w(smem_u32(&s.bar_s_full[0]));
+        issue_dp(0);
+        mma_commit_w(smem_u32(&s.bar_dp_full));
+      }
+      if (ok && N > 1) {
+        ok = mbar_wait_warp(smem_u32(&s.bar_q_full[1 % STAGES]), 0, wc, TAG_Q_FULL);
         tc_fence_after();
-        const uint32_t colS = tbase + COL_S + bf * 128;
-        const uint32_t sQ = smem_u32(s.Q[st]), sdO = smem_u32(s.dO[st]);
-#pragma unroll
-        for (int kk = 0; kk < HEAD_DIM / 16; ++kk) {
-          const uint32_t ao = (kk >> 2) * (KV_TILE * 128) + (kk & 3) * 32;
-          const uint32_t bo = (kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32;
-          mma_ss(colS, sdesc_sw128(sK + ao, 16, 1024), sdesc_sw128(sQ + bo, 16, 1024), ID_S,
-                 kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < HEAD_DIM / 16; ++kk) {
-          const uint32_t ao = (kk >> 2) * (KV_TILE * 128) + (kk & 3) * 32;
-          const uint32_t bo = (kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32;
-          mma_ss(colS + 64, sdesc_sw128(sV + ao, 16, 1024), sdesc_sw128(sdO + bo, 16, 1024), ID_S,
-                 kk > 0 ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&s.bar_s_full[bf]));
-        if (n >= 1 && !consume(n - 1)) {
-          ok = false;
-          break;
+        if (ok) {
+          issue_s(1);
+          mma_commit_w(smem_u32(&s.bar_s_full[1]));
         }
       }
-      if (ok && N >= 1) ok = consume(N - 1);
-      mma_commit(smem_u32(&s.bar_acc_full));
-      mma_commit(smem_u32(&s.bar_drain));
-      mbar_wait(smem_u32(&s.bar_drain), 0, wc, TAG_DRAIN);
     }
+    for (int n = 0; ok && n < N; ++n) {
+      const int bf = n & 1;
+      ok = mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), (n >> 1) & 1, wc, TAG_P_FULL);
+      if (!ok) break;
+      tc_fence_after();
+      issue_acc(n, false);  // dV += P^T dO
+      ok = mbar_wait_warp(smem_u32(&s.bar_ds_full), n & 1, wc, TAG_DS_FULL);
+      if (!ok) break;
+      tc_fence_after();
+      issue_acc(n, true);   // dK += dS^T Q
+      mma_commit_w(smem_u32(&s.bar_q_empty[n % STAGES]));
+      mma_commit_w(smem_u32(&s.bar_st_free[bf]));
+      if (n + 1 < N) {
+        // the softmax warps have read dP^T(n) (ds_full); Q/dO of step n + 1
+        // were waited for before S(n + 1)
+        issue_dp(n + 1);
+        mma_commit_w(smem_u32(&s.bar_dp_full));
+      }
+      const int m = n + 2;
+      if (m < N) {
+        ok = mbar_wait_warp(smem_u32(&s.bar_q_full[m % STAGES]), (m / STAGES) & 1, wc,
+                            TAG_Q_FULL) &&
+             mbar_wait_warp(smem_u32(&s.bar_st_free[bf]), (n >> 1) & 1, wc, TAG_ST_FREE);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(m);  // overwrites P^T(n) / dS^T(n), which dV(n) / dK(n) have read
+        mma_commit_w(smem_u32(&s.bar_s_full[bf]));
+      }
+    }
+    // completes when every MMA issued above has (also on the abort path, so
+    // that TMEM is idle before it is freed)
+    mma_commit_w(smem_u32(&s.bar_acc_full));
+    mbar_wait_warp(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
   } else {
     // ------------------------------------------------------------ softmax warps
     const int sp = warp & 3, g = (warp - 2) >> 2;
     const int rloc = sp * 32 + lane;
     const int j = k0 + rloc;
     const uint32_t lane_base = tbase + ((uint32_t)(sp * 32) << 16);
-    bool ok = true;
+    bool ok = mbar_wait(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV);
+    if (ok) {
+      // K rows into TMEM as 16-bit pairs (element 2c in the low half of column
+      // c): this warp copies d columns 64 g .. 64 g + 63 of its rows.
+      const uint8_t* src = s.K + g * (KV_TILE * 128) + rloc * 128;
+      uint32_t w[32];
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + ((cc ^ (rloc & 7)) << 4));
+        w[4 * cc] = v.x;
+        w[4 * cc + 1] = v.y;
+        w[4 * cc + 2] = v.z;
+        w[4 * cc + 3] = v.w;
+      }
+      tmem_st32(lane_base + COL_KA + 32 * g, w);
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&s.bar_ka_full));
+
     KVCursor cur;
     cur.start(p, walk);
-    for (int n = 0; n < N; ++n) {
-      const int bf = n % NBUF, st = n % STAGES;
+    for (int n = 0; ok && n < N; ++n) {
+      const int bf = n & 1, st = n % STAGES;
+      const uint32_t col = COL_ST + 64 * bf + 32 * g;
       // s_full implies the stage's loads landed; waiting on q_full as well
       // makes the bulk-copied lse2 / Delta rows visible to this thread
-      if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (n / NBUF) & 1, wc, TAG_S_FULL) ||
+      if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (n >> 1) & 1, wc, TAG_S_FULL) ||
           !mbar_wait(smem_u32(&s.bar_q_full[st]), (n / STAGES) & 1, wc, TAG_Q_FULL)) {
         ok = false;
         break;
@@ -232,47 +298,66 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       const int bh = b * p.Hq + c * p.group + cur.hh;
       cur.next(p, walk);
       const uint32_t vis = vis_key_row(p, bh, j, r * KV_SUB + 32 * g);
-      const uint32_t col = COL_S + bf * 128 + 32 * g;
-      float sv[32], dp[32];
-      tmem_ld32(lane_base + col, sv);
-      tmem_ld32(lane_base + col + 64, dp);
-      tmem_wait_ld();
-      const float4* l4 = reinterpret_cast<const float4*>(&s.lse2[st][32 * g]);
-      const float4* d4 = reinterpret_cast<const float4*>(&s.delta[st][32 * g]);
-      uint32_t pkP[16], pkD[16];
+      float pv[32];
+      {
+        float sv[32];
+        tmem_ld32(lane_base + col, sv);
+        tmem_wait_ld();
+        const float4* l4 = reinterpret_cast<const float4*>(&s.lse2[st][32 * g]);
+        uint32_t pk[16];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 L = l4[q], Dl = d4[q];
-        const float lv[4] = {L.x, L.y, L.z, L.w};
-        const float dv4[4] = {Dl.x, Dl.y, Dl.z, Dl.w};
-        float pv[4], dsv[4];
+        for (int q = 0; q < 8; ++q) {
+          const float4 L = l4[q];
+          const float lv[4] = {L.x, L.y, L.z, L.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int cc = 4 * q + e;
-          float pe = fast_exp2(fmaf(sv[cc], p.scale_log2, -lv[e]));
-          pe = ((vis >> cc) & 1u) ? pe : 0.f;
-          pv[e] = pe;
-          dsv[e] = pe * (dp[cc] - dv4[e]);
+          for (int e = 0; e < 4; ++e) {
+            const int cc = 4 * q + e;
+            const float pe = fast_exp2(fmaf(sv[cc], p.scale_log2, -lv[e]));
+            pv[cc] = ((vis >> cc) & 1u) ? pe : 0.f;
+          }
+          pk[2 * q] = pack2<BF16>(pv[4 * q], pv[4 * q + 1]);
+          pk[2 * q + 1] = pack2<BF16>(pv[4 * q + 2], pv[4 * q + 3]);
         }
-        pkP[2 * q] = pack2<BF16>(pv[0], pv[1]);
-        pkP[2 * q + 1] = pack2<BF16>(pv[2], pv[3]);
-        pkD[2 * q] = pack2<BF16>(dsv[0], dsv[1]);
-        pkD[2 * q + 1] = pack2<BF16>(dsv[2], dsv[3]);
+        tmem_st16(lane_base + col, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.bar_p_full[bf]));
       }
-      tmem_st16(lane_base + col, pkP);
-      tmem_st16(lane_base + col + 64, pkD);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s.bar_p_full[bf]));
+      if (!mbar_wait(smem_u32(&s.bar_dp_full), n & 1, wc, TAG_DP_FULL)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        float dp[32];
+        tmem_ld32(lane_base + COL_DPT + 32 * g, dp);
+        tmem_wait_ld();
+        const float4* d4 = reinterpret_cast<const float4*>(&s.delta[st][32 * g]);
+        uint32_t pk[16];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 D = d4[q];
+          pk[2 * q] = pack2<BF16>(pv[4 * q] * (dp[4 * q] - D.x), pv[4 * q + 1] * (dp[4 * q + 1] - D.y));
+          pk[2 * q + 1] =
+              pack2<BF16>(pv[4 * q + 2] * (dp[4 * q + 2] - D.z), pv[4 * q + 3] * (dp[4 * q + 3] - D.w));
+        }
+        tmem_st16(lane_base + col + 16, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.bar_ds_full));
+      }
     }
     // ---------------------------------------------------------- epilogue
     bool have = ok && N > 0;
     if (have) have = mbar_wait(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
     tc_fence_after();
+    // K in shared memory is dead once every softmax warp has copied it
+    named_bar_sync(1, 256);
     const int r0 = k0 + sp * 32;
     const int nvalid = min(32, p.Skv - r0);
-    uint8_t* stage = &s.Q[0][0] + (warp - 2) * 4096;  // Q stages are idle now
+    uint8_t* stage = s.K + (warp - 2) * 4096;
 #pragma unroll 1
     for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
       uint32_t pk[32];
