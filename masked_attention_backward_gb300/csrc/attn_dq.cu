@@ -23,17 +23,23 @@
 //
 // TMEM columns (512): dQ accumulator [0,128), Q [128,192), dO [192,256)
 // (16-bit pairs), and two S/dP buffers of 128 columns at 256 and 384 (S in
-// the first 64, dP in the next 64; dS is packed over the start of S).
+// the first 64, dP in the next 64).  Softmax group g owns key columns
+// 16 g .. 16 g + 15 and packs its 16 dS values over the first 8 of them, so
+// the 16 keys of MMA K-step g sit at buffer column 16 g.
 //
-// MMA order: dQ(n), then dP(n+2) into the dP half of the buffer dQ(n) is not
-// reading, then -- once dQ(n) has completed -- S(n+2) over dS(n).  The wait
-// for dQ(n) is covered by dP(n+2) already queued behind it, so the tensor
-// pipe never drains between steps.
+// Two warps issue MMAs into the one tensor pipe: warp 1 the score products
+// S(m), dP(m), warp 2 the accumulation dQ(n).  The pipe accepts only a few
+// MMAs ahead of the one executing and a barrier wait costs a few hundred
+// cycles while the softmax warps keep the SM busy, so with a single issuer
+// every wait drained the pipe; with two, one warp's MMAs keep it fed while
+// the other waits.  S(m) / dP(m) wait for dQ(m-2), which read dS(m-2) from
+// the same buffer; dQ(n) waits for the softmax warps' dS(n).
 //
-// Warp roles (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues the MMAs (whole warp, one elected lane), warps 2..9 are two groups
-// of four warps; warp (sp, g) owns TMEM lanes 32 sp .. 32 sp + 31 and key
-// columns 32 g .. 32 g + 31 of each sub-tile.
+// Warp roles (608 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues S / dP, warp 2 issues dQ (both whole warps, one elected lane), warps
+// 3..18 are four groups of four softmax warps; warp (sp, g) with sp = warp % 4
+// owns TMEM lanes 32 sp .. 32 sp + 31 (query rows) and key columns
+// 16 g .. 16 g + 15 of each sub-tile.
 #include <math.h>
 
 #include "tiles.cuh"
@@ -42,34 +48,47 @@ namespace mab {
 
 namespace dq_side {
 
-constexpr int STAGES = 4;     // K/V ring depth
+constexpr int STAGES = 6;     // K/V ring depth; stages 4 and 5 reuse the Q / dO tiles
 constexpr int COL_ACC = 0;    // dQ accumulator, 128 fp32 columns
 constexpr int COL_QA = 128;   // Q as the A operand, 64 columns of 16-bit pairs
 constexpr int COL_DOA = 192;  // dO as the A operand
 constexpr int COL_BUF = 256;  // buffer b: S at COL_BUF + 128 b, dP at +64
-constexpr int NUM_THREADS = 320;
+constexpr int SM_WARPS = 16;   // softmax warps
+constexpr int SM_WARP0 = 3;     // first softmax warp
+constexpr int NUM_THREADS = 32 * (SM_WARP0 + SM_WARPS);
 
 struct __align__(1024) Smem {
-  uint8_t Q[2 * Q_TILE * 128];  // two 64-column chunks, 128B swizzle
-  uint8_t dO[2 * Q_TILE * 128];
-  uint8_t K[STAGES][2 * Q_SUB * 128];
-  uint8_t V[STAGES][2 * Q_SUB * 128];
+  uint8_t Q[2 * Q_TILE * 128];  // two 64-column chunks, 128B swizzle; later K/V stage 4
+  uint8_t dO[2 * Q_TILE * 128]; // later K/V stage 5
+  uint8_t K[STAGES - 2][2 * Q_SUB * 128];
+  uint8_t V[STAGES - 2][2 * Q_SUB * 128];
   uint64_t bar_q_full;          // Q, dO landed in shared memory
-  uint64_t bar_qa_full;         // Q, dO copied into TMEM (8 softmax warps)
+  uint64_t bar_qa_full;         // Q, dO copied into TMEM (all softmax warps)
   uint64_t bar_kv_full[STAGES];
   uint64_t bar_kv_empty[STAGES];
   uint64_t bar_s_full[2];       // S and dP of the buffer complete
-  uint64_t bar_p_full[2];       // dS of the buffer packed (8 softmax warps)
+  uint64_t bar_p_full[2];       // dS of the buffer packed (all softmax warps)
   uint64_t bar_acc_free[2];     // dQ MMA that read the buffer's dS complete
+  uint64_t bar_x_done;          // every S / dP MMA complete
   uint64_t bar_acc_full;
   uint32_t tmem_base;
   int abort_flag;
 };
 
 constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
+static_assert(2 * Q_TILE * 128 == 2 * (2 * Q_SUB * 128), "a K/V stage must fit in a Q tile");
+
+// K / V tile of stage st (stages 4 and 5 live in the Q and dO tiles once
+// those are in TMEM).
+__device__ __forceinline__ uint8_t* stage_k(Smem& s, int st) {
+  return st < STAGES - 2 ? s.K[st] : (st == STAGES - 2 ? s.Q : s.dO);
+}
+__device__ __forceinline__ uint8_t* stage_v(Smem& s, int st) {
+  return st < STAGES - 2 ? s.V[st] : (st == STAGES - 2 ? s.Q : s.dO) + 2 * Q_SUB * 128;
+}
 
 enum { TAG_Q = 0x301, TAG_QA, TAG_KV_EMPTY, TAG_KV_FULL, TAG_P_FULL, TAG_S_FULL, TAG_ACC_FREE,
-       TAG_ACC };
+       TAG_ACC, TAG_X_DONE };
 
 }  // namespace dq_side
 
@@ -97,16 +116,17 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
     mbar_init(smem_u32(&s.bar_q_full), 1);
-    mbar_init(smem_u32(&s.bar_qa_full), 8);
+    mbar_init(smem_u32(&s.bar_qa_full), SM_WARPS);
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_u32(&s.bar_kv_full[i]), 1);
       mbar_init(smem_u32(&s.bar_kv_empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_s_full[i]), 1);
-      mbar_init(smem_u32(&s.bar_p_full[i]), 8);
+      mbar_init(smem_u32(&s.bar_p_full[i]), SM_WARPS);
       mbar_init(smem_u32(&s.bar_acc_free[i]), 1);
     }
+    mbar_init(smem_u32(&s.bar_x_done), 1);
     mbar_init(smem_u32(&s.bar_acc_full), 1);
     fence_mbar_init();
   }
@@ -137,109 +157,107 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         if (n >= STAGES &&
             !mbar_wait(smem_u32(&s.bar_kv_empty[st]), ((n / STAGES) - 1) & 1, wc, TAG_KV_EMPTY))
           break;
+        // stages 4 and 5 overwrite the Q / dO tiles: wait until every softmax
+        // warp has copied them into TMEM
+        if (n == STAGES - 2 && !mbar_wait(smem_u32(&s.bar_qa_full), 0, wc, TAG_QA)) break;
         const int t = walk.tile(n);
         const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
+        uint8_t* sk = stage_k(s, st);
+        uint8_t* sv = stage_v(s, st);
         mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
-        tma_load_3d(smem_u32(s.K[st]), &tK, 0, t * Q_SUB, kvh, fb);
-        tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, t * Q_SUB, kvh, fb);
-        tma_load_3d(smem_u32(s.V[st]), &tV, 0, t * Q_SUB, kvh, fb);
-        tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, t * Q_SUB, kvh, fb);
+        tma_load_3d(smem_u32(sk), &tK, 0, t * Q_SUB, kvh, fb);
+        tma_load_3d(smem_u32(sk + Q_SUB * 128), &tK, 64, t * Q_SUB, kvh, fb);
+        tma_load_3d(smem_u32(sv), &tV, 0, t * Q_SUB, kvh, fb);
+        tma_load_3d(smem_u32(sv + Q_SUB * 128), &tV, 64, t * Q_SUB, kvh, fb);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (whole warp)
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers (whole warps)
     constexpr uint32_t ID_S = idesc_f16(BF16, Q_TILE, Q_SUB, false, false);
     constexpr uint32_t ID_ACC = idesc_f16(BF16, Q_TILE, HEAD_DIM, false, true);
-    // S(m) = Q K^T into buffer m & 1 (A = Q from TMEM, B = K tile, K-major)
-    auto issue_s = [&](int m) {
-      const uint32_t d = tbase + COL_BUF + (m & 1) * 128;
-      const uint64_t bK = sdesc_sw128(smem_u32(s.K[m % STAGES]), 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-        mma_ts_w(d, tbase + COL_QA + 8 * kk,
-                 bK + (uint64_t)(((kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                 kk > 0 ? 1u : 0u);
-    };
-    // dP(m) = dO V^T into the dP half of buffer m & 1
-    auto issue_dp = [&](int m) {
-      const uint32_t d = tbase + COL_BUF + (m & 1) * 128 + 64;
-      const uint64_t bV = sdesc_sw128(smem_u32(s.V[m % STAGES]), 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-        mma_ts_w(d, tbase + COL_DOA + 8 * kk,
-                 bV + (uint64_t)(((kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                 kk > 0 ? 1u : 0u);
-    };
-    // dQ += dS(m) K (A = dS packed in buffer m & 1, B = K tile, MN-major)
-    auto issue_dq = [&](int m) {
-      const uint32_t a = tbase + COL_BUF + (m & 1) * 128;
-      const uint64_t bK = sdesc_sw128(smem_u32(s.K[m % STAGES]), Q_SUB * 128, 1024);
-#pragma unroll
-      for (int kk = 0; kk < Q_SUB / 16; ++kk)
-        mma_ts_w(tbase + COL_ACC, a + 32 * (kk >> 1) + 8 * (kk & 1),
-                 bK + (uint64_t)((kk * 2048) >> 4), ID_ACC, (m > 0 || kk > 0) ? 1u : 0u);
-    };
-    bool ok = N == 0 || mbar_wait_warp(smem_u32(&s.bar_qa_full), 0, wc, TAG_QA);
-    tc_fence_after();
-    for (int m = 0; ok && m < N && m < 2; ++m) {
-      ok = mbar_wait_warp(smem_u32(&s.bar_kv_full[m % STAGES]), (m / STAGES) & 1, wc, TAG_KV_FULL);
-      if (!ok) break;
-      tc_fence_after();
-      issue_s(m);
-      issue_dp(m);
-      mma_commit_w(smem_u32(&s.bar_s_full[m & 1]));
-    }
-    for (int n = 0; ok && n < N; ++n) {
-      const int bf = n & 1;
-      ok = mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), (n >> 1) & 1, wc, TAG_P_FULL);
-      if (!ok) break;
-      tc_fence_after();
-      issue_dq(n);
-      mma_commit_w(smem_u32(&s.bar_kv_empty[n % STAGES]));
-      mma_commit_w(smem_u32(&s.bar_acc_free[bf]));
-      const int m = n + 2;
-      if (m < N) {
-        ok = mbar_wait_warp(smem_u32(&s.bar_kv_full[m % STAGES]), (m / STAGES) & 1, wc,
-                            TAG_KV_FULL);
+    if (warp == 1) {
+      // S(m) = Q K^T and dP(m) = dO V^T into buffer m & 1 (A = Q / dO from TMEM,
+      // B = K / V tile, K-major)
+      bool ok = N == 0 || mbar_wait_warp(smem_u32(&s.bar_qa_full), 0, wc, TAG_QA);
+      for (int m = 0; ok && m < N; ++m) {
+        const int bf = m & 1, st = m % STAGES;
+        ok = mbar_wait_warp(smem_u32(&s.bar_kv_full[st]), (m / STAGES) & 1, wc, TAG_KV_FULL);
+        // the buffer held dS(m - 2) (read by dQ(m - 2)) and dP(m - 2) (read by
+        // the softmax warps before they signalled step m - 2)
+        if (ok && m >= 2)
+          ok = mbar_wait_warp(smem_u32(&s.bar_acc_free[bf]), ((m - 2) >> 1) & 1, wc,
+                              TAG_ACC_FREE);
         if (!ok) break;
         tc_fence_after();
-        issue_dp(m);  // the dP half was last read by the softmax warps of step n
-        ok = mbar_wait_warp(smem_u32(&s.bar_acc_free[bf]), (n >> 1) & 1, wc, TAG_ACC_FREE);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s(m);  // overwrites dS(n), which dQ(n) has finished reading
+        const uint32_t d = tbase + COL_BUF + bf * 128;
+        const uint64_t bK = sdesc_sw128(smem_u32(stage_k(s, st)), 16, 1024);
+        const uint64_t bV = sdesc_sw128(smem_u32(stage_v(s, st)), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+          mma_ts_w(d, tbase + COL_QA + 8 * kk,
+                   bK + (uint64_t)(((kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                   kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+          mma_ts_w(d + 64, tbase + COL_DOA + 8 * kk,
+                   bV + (uint64_t)(((kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                   kk > 0 ? 1u : 0u);
         mma_commit_w(smem_u32(&s.bar_s_full[bf]));
       }
+      // this warp's MMAs must be complete before TMEM is freed (abort path)
+      mma_commit_w(smem_u32(&s.bar_x_done));
+      mbar_wait_warp(smem_u32(&s.bar_x_done), 0, wc, TAG_X_DONE);
+    } else {
+      // dQ += dS(n) K (A = dS packed in buffer n & 1, B = K tile, MN-major)
+      bool ok = true;
+      for (int n = 0; ok && n < N; ++n) {
+        const int bf = n & 1, st = n % STAGES;
+        ok = mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), (n >> 1) & 1, wc, TAG_P_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a = tbase + COL_BUF + bf * 128;
+        const uint64_t bK = sdesc_sw128(smem_u32(stage_k(s, st)), Q_SUB * 128, 1024);
+#pragma unroll
+        for (int kk = 0; kk < Q_SUB / 16; ++kk)
+          mma_ts_w(tbase + COL_ACC, a + 16 * kk, bK + (uint64_t)((kk * 2048) >> 4), ID_ACC,
+                   (n > 0 || kk > 0) ? 1u : 0u);
+        // S(n) and dP(n) completed before the softmax warps could signal step
+        // n, so this commit also frees the K / V stage
+        mma_commit_w(smem_u32(&s.bar_kv_empty[st]));
+        mma_commit_w(smem_u32(&s.bar_acc_free[bf]));
+      }
+      // completes when every MMA issued above has (also on the abort path, so
+      // that TMEM is idle before it is freed)
+      mma_commit_w(smem_u32(&s.bar_acc_full));
+      mbar_wait_warp(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
     }
-    // completes when every MMA issued above has (also on the abort path, so
-    // that TMEM is idle before it is freed)
-    mma_commit_w(smem_u32(&s.bar_acc_full));
-    mbar_wait_warp(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int sp = warp & 3, g = (warp - 2) >> 2;
+    const int sp = warp & 3, g = (warp - SM_WARP0) >> 2;
     const int rloc = sp * 32 + lane;
     const int i = q0 + rloc;
     const uint32_t lane_base = tbase + ((uint32_t)(sp * 32) << 16);
     bool ok = mbar_wait(smem_u32(&s.bar_q_full), 0, wc, TAG_Q);
     if (ok) {
       // Q and dO rows into TMEM as 16-bit pairs (element 2c in the low half
-      // of column c): this warp copies d columns 64 g .. 64 g + 63 of its rows.
-      const uint8_t* src[2] = {s.Q + g * (Q_TILE * 128) + rloc * 128,
-                               s.dO + g * (Q_TILE * 128) + rloc * 128};
-      const uint32_t dst[2] = {COL_QA + 32u * g, COL_DOA + 32u * g};
+      // of column c): this warp copies d columns 32 g .. 32 g + 31 of its rows.
+      const int chunk = g >> 1, u0 = (g & 1) * 4;
+      const uint8_t* src[2] = {s.Q + chunk * (Q_TILE * 128) + rloc * 128,
+                               s.dO + chunk * (Q_TILE * 128) + rloc * 128};
+      const uint32_t dst[2] = {COL_QA + 16u * g, COL_DOA + 16u * g};
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        uint32_t w[32];
+        uint32_t w[16];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src[which] + ((c ^ (rloc & 7)) << 4));
-          w[4 * c] = v.x;
-          w[4 * c + 1] = v.y;
-          w[4 * c + 2] = v.z;
-          w[4 * c + 3] = v.w;
+        for (int u = 0; u < 4; ++u) {
+          const uint4 v =
+              *reinterpret_cast<const uint4*>(src[which] + (((u0 + u) ^ (rloc & 7)) << 4));
+          w[4 * u] = v.x;
+          w[4 * u + 1] = v.y;
+          w[4 * u + 2] = v.z;
+          w[4 * u + 3] = v.w;
         }
-        tmem_st32(lane_base + dst[which], w);
+        tmem_st16(lane_base + dst[which], w);
       }
       tmem_wait_st();
     }
@@ -258,54 +276,63 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       }
       tc_fence_after();
       const int t = walk.tile(n);
-      const uint32_t vis = vis_query_row(p, bh, i, t * Q_SUB + 32 * g);
-      const uint32_t col = COL_BUF + bf * 128 + 32 * g;
-      float sv[32], dp[32];
-      tmem_ld32(lane_base + col, sv);
-      tmem_ld32(lane_base + col + 64, dp);
-      tmem_wait_ld();
-      uint32_t pk[16];
+      const uint32_t col = COL_BUF + bf * 128 + 16 * g;
+      float sv[16], dp[16];
+      tmem_ld16(lane_base + col, sv);
+      tmem_ld16(lane_base + col + 64, dp);
+      // warp-uniform: the whole 128 x 64 sub-tile is visible
+      const bool full = tile_all_visible(p, q0, Q_TILE, t * Q_SUB, Q_SUB);
+      const uint32_t vis = full ? 0xffffu : vis_query_row(p, bh, i, t * Q_SUB + 16 * g);
+      tmem_wait_ld_regs(sv);
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -lse2_i));
-        float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -lse2_i));
-        p0 = ((vis >> (2 * c)) & 1u) ? p0 : 0.f;
-        p1 = ((vis >> (2 * c + 1)) & 1u) ? p1 : 0.f;
-        pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
+      for (int c = 0; c < 16; ++c) asm volatile("" : "+f"(dp[c]));
+      uint32_t pk[8];
+      if (full) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -lse2_i));
+          const float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -lse2_i));
+          pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -lse2_i));
+          float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -lse2_i));
+          p0 = ((vis >> (2 * c)) & 1u) ? p0 : 0.f;
+          p1 = ((vis >> (2 * c + 1)) & 1u) ? p1 : 0.f;
+          pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
+        }
       }
-      tmem_st16(lane_base + col, pk);
+      tmem_st8(lane_base + col, pk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s.bar_p_full[bf]));
     }
     // ---------------------------------------------------------- epilogue
-    // Columns [64 g, 64 g + 64) of the accumulator, one row per lane.
-    uint32_t pk[32];
+    // Columns [32 g, 32 g + 32) of the accumulator, one row per lane.
+    uint32_t pk[16];
     bool have = ok && N > 0;
     if (have) have = mbar_wait(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
     tc_fence_after();
     if (have) {
+      float v[32];
+      tmem_ld32(lane_base + COL_ACC + 32 * g, v);
+      tmem_wait_ld_regs(v);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float v[32];
-        tmem_ld32(lane_base + COL_ACC + 64 * g + 32 * half, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          pk[16 * half + c] = pack2<BF16>(v[2 * c] * p.scale, v[2 * c + 1] * p.scale);
-      }
+      for (int c = 0; c < 16; ++c) pk[c] = pack2<BF16>(v[2 * c] * p.scale, v[2 * c + 1] * p.scale);
     } else {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = 0u;
+      for (int c = 0; c < 16; ++c) pk[c] = 0u;
     }
-    // The Q tile in shared memory is dead once it is in TMEM (every softmax
-    // warp passed its copy before reaching here); it stages the output rows.
-    named_bar_sync(1, 256);
-    uint8_t* stage = s.Q + (warp - 2) * 4096;
+    // Every MMA has completed (or none was issued), so no stage is being
+    // read or loaded: the first two K tiles stage the output rows.
+    named_bar_sync(1, 32 * SM_WARPS);
+    uint8_t* stage = s.K[0] + (warp - SM_WARP0) * 2048;
     const int r0 = q0 + sp * 32;
-    uint16_t* orow = dq + ((size_t)bh * p.Sq + r0) * HEAD_DIM + 64 * g;
-    warp_store_rows(stage, pk, orow, min(32, p.Sq - r0));
+    uint16_t* orow = dq + ((size_t)bh * p.Sq + r0) * HEAD_DIM + 32 * g;
+    warp_store_rows32(stage, pk, orow, min(32, p.Sq - r0));
   }
   tc_fence_before();
   __syncthreads();

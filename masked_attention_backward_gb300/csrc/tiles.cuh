@@ -62,6 +62,25 @@ __device__ __forceinline__ uint32_t vis_key_row(const AttnParams& p, int bh, int
   }
 }
 
+// True when every pair (i, j) with i in [i0, i0 + ni), j in [j0, j0 + nj) is
+// in range and visible under a closed-form mask (never for block masks,
+// whose tiles take the per-thread bitmask path).  Lets a whole sub-tile skip
+// the per-element visibility select.
+__device__ __forceinline__ bool tile_all_visible(const AttnParams& p, int i0, int ni, int j0,
+                                                 int nj) {
+  if (i0 + ni > p.Sq || j0 + nj > p.Skv) return false;
+  switch (p.mask_kind) {
+    case MK_NONE:
+      return true;
+    case MK_CAUSAL:
+      return i0 >= j0 + nj - 1;
+    case MK_SLIDING:
+      return i0 >= j0 + nj - 1 && (i0 + ni - 1) - j0 < p.window;
+    default:
+      return false;
+  }
+}
+
 // Walk of a query-tile CTA (Q_TILE rows of head bh) over key sub-tiles of
 // Q_SUB rows.
 struct QWalk {
@@ -163,6 +182,29 @@ __device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint32_t (
   for (int k = 0; k < 8; ++k) {
     int row = k * 4 + (lane >> 3), c = lane & 7;
     uint4 v = *reinterpret_cast<const uint4*>(stage + row * 128 + ((c ^ (row & 7)) << 4));
+    if (row < nvalid) *reinterpret_cast<uint4*>(out_row0 + (size_t)row * HEAD_DIM + c * 8) = v;
+  }
+  __syncwarp();
+}
+
+// Store 32 rows x 32 columns (16-bit elements, packed as 16 u32 per lane, one
+// row per lane) through a per-warp 2 KB staging buffer, so that each global
+// store instruction writes 8 rows of 64 contiguous bytes.  out_row0 points at
+// column col0 of the warp's first row; row stride is HEAD_DIM elements; rows
+// >= nvalid are skipped.
+__device__ __forceinline__ void warp_store_rows32(uint8_t* stage, const uint32_t (&pk)[16],
+                                                  uint16_t* out_row0, int nvalid) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    *reinterpret_cast<uint4*>(stage + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = v;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    int row = k * 8 + (lane >> 2), c = lane & 3;
+    uint4 v = *reinterpret_cast<const uint4*>(stage + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
     if (row < nvalid) *reinterpret_cast<uint4*>(out_row0 + (size_t)row * HEAD_DIM + c * 8) = v;
   }
   __syncwarp();
