@@ -27,19 +27,19 @@
 // 16 g .. 16 g + 15 and packs its 16 dS values over the first 8 of them, so
 // the 16 keys of MMA K-step g sit at buffer column 16 g.
 //
-// Two warps issue MMAs into the one tensor pipe: warp 1 the score products
-// S(m), dP(m), warp 2 the accumulation dQ(n).  The pipe accepts only a few
-// MMAs ahead of the one executing and a barrier wait costs a few hundred
-// cycles while the softmax warps keep the SM busy, so with a single issuer
-// every wait drained the pipe; with two, one warp's MMAs keep it fed while
-// the other waits.  S(m) / dP(m) wait for dQ(m-2), which read dS(m-2) from
-// the same buffer; dQ(n) waits for the softmax warps' dS(n).
+// Three warps issue MMAs into the one tensor pipe: warp 1 S(m), warp 2 dP(m),
+// warp 3 the accumulation dQ(n).  The pipe accepts only a few MMAs ahead of
+// the one executing and a barrier wait costs a few hundred cycles while the
+// softmax warps keep the SM busy, so with a single issuer every wait drained
+// the pipe; with several, one warp's MMAs keep it fed while another waits.
+// S(m) waits for dQ(m-2), which read dS(m-2) from the same buffer; dP(m)
+// waits for the softmax warps to have read dP(m-2); dQ(n) waits for dS(n).
 //
-// Warp roles (608 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues S / dP, warp 2 issues dQ (both whole warps, one elected lane), warps
-// 3..18 are four groups of four softmax warps; warp (sp, g) with sp = warp % 4
-// owns TMEM lanes 32 sp .. 32 sp + 31 (query rows) and key columns
-// 16 g .. 16 g + 15 of each sub-tile.
+// Warp roles (640 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues S, warp 2 issues dP, warp 3 issues dQ (whole warps, one elected
+// lane), warps 4..19 are four groups of four softmax warps; warp (sp, g) with
+// sp = warp % 4 owns TMEM lanes 32 sp .. 32 sp + 31 (query rows) and key
+// columns 16 g .. 16 g + 15 of each sub-tile.
 #include <math.h>
 
 #include "tiles.cuh"
@@ -54,7 +54,7 @@ constexpr int COL_QA = 128;   // Q as the A operand, 64 columns of 16-bit pairs
 constexpr int COL_DOA = 192;  // dO as the A operand
 constexpr int COL_BUF = 256;  // buffer b: S at COL_BUF + 128 b, dP at +64
 constexpr int SM_WARPS = 16;   // softmax warps
-constexpr int SM_WARP0 = 3;     // first softmax warp
+constexpr int SM_WARP0 = 4;     // first softmax warp
 constexpr int NUM_THREADS = 32 * (SM_WARP0 + SM_WARPS);
 
 struct __align__(1024) Smem {
@@ -66,10 +66,10 @@ struct __align__(1024) Smem {
   uint64_t bar_qa_full;         // Q, dO copied into TMEM (all softmax warps)
   uint64_t bar_kv_full[STAGES];
   uint64_t bar_kv_empty[STAGES];
-  uint64_t bar_s_full[2];       // S and dP of the buffer complete
+  uint64_t bar_s_full[2];       // S and dP of the buffer complete (one commit each)
   uint64_t bar_p_full[2];       // dS of the buffer packed (all softmax warps)
   uint64_t bar_acc_free[2];     // dQ MMA that read the buffer's dS complete
-  uint64_t bar_x_done;          // every S / dP MMA complete
+  uint64_t bar_x_done[2];       // every S (0) / dP (1) MMA complete
   uint64_t bar_acc_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -122,11 +122,12 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       mbar_init(smem_u32(&s.bar_kv_empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&s.bar_s_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_s_full[i]), 2);
       mbar_init(smem_u32(&s.bar_p_full[i]), SM_WARPS);
       mbar_init(smem_u32(&s.bar_acc_free[i]), 1);
     }
-    mbar_init(smem_u32(&s.bar_x_done), 1);
+    mbar_init(smem_u32(&s.bar_x_done[0]), 1);
+    mbar_init(smem_u32(&s.bar_x_done[1]), 1);
     mbar_init(smem_u32(&s.bar_acc_full), 1);
     fence_mbar_init();
   }
@@ -171,42 +172,41 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         tma_load_3d(smem_u32(sv + Q_SUB * 128), &tV, 64, t * Q_SUB, kvh, fb);
       }
     }
-  } else if (warp == 1 || warp == 2) {
+  } else if (warp >= 1 && warp < SM_WARP0) {
     // ------------------------------------------------------------ MMA issuers (whole warps)
     constexpr uint32_t ID_S = idesc_f16(BF16, Q_TILE, Q_SUB, false, false);
     constexpr uint32_t ID_ACC = idesc_f16(BF16, Q_TILE, HEAD_DIM, false, true);
-    if (warp == 1) {
-      // S(m) = Q K^T and dP(m) = dO V^T into buffer m & 1 (A = Q / dO from TMEM,
-      // B = K / V tile, K-major)
+    if (warp == 1 || warp == 2) {
+      // warp 1: S(m) = Q K^T into the S half of buffer m & 1; warp 2: dP(m) =
+      // dO V^T into its dP half (A = Q / dO from TMEM, B = K / V tile, K-major)
+      const bool is_s = warp == 1;
+      const uint32_t a0 = tbase + (is_s ? COL_QA : COL_DOA);
       bool ok = N == 0 || mbar_wait_warp(smem_u32(&s.bar_qa_full), 0, wc, TAG_QA);
       for (int m = 0; ok && m < N; ++m) {
         const int bf = m & 1, st = m % STAGES;
         ok = mbar_wait_warp(smem_u32(&s.bar_kv_full[st]), (m / STAGES) & 1, wc, TAG_KV_FULL);
-        // the buffer held dS(m - 2) (read by dQ(m - 2)) and dP(m - 2) (read by
-        // the softmax warps before they signalled step m - 2)
-        if (ok && m >= 2)
-          ok = mbar_wait_warp(smem_u32(&s.bar_acc_free[bf]), ((m - 2) >> 1) & 1, wc,
-                              TAG_ACC_FREE);
+        if (ok && m >= 2) {
+          // S half: held dS(m - 2), read by dQ(m - 2); dP half: read by the
+          // softmax warps before they signalled step m - 2
+          ok = is_s ? mbar_wait_warp(smem_u32(&s.bar_acc_free[bf]), ((m - 2) >> 1) & 1, wc,
+                                     TAG_ACC_FREE)
+                    : mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), ((m - 2) >> 1) & 1, wc,
+                                     TAG_P_FULL);
+        }
         if (!ok) break;
         tc_fence_after();
-        const uint32_t d = tbase + COL_BUF + bf * 128;
-        const uint64_t bK = sdesc_sw128(smem_u32(stage_k(s, st)), 16, 1024);
-        const uint64_t bV = sdesc_sw128(smem_u32(stage_v(s, st)), 16, 1024);
+        const uint32_t d = tbase + COL_BUF + bf * 128 + (is_s ? 0 : 64);
+        const uint64_t bB = sdesc_sw128(smem_u32(is_s ? stage_k(s, st) : stage_v(s, st)), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-          mma_ts_w(d, tbase + COL_QA + 8 * kk,
-                   bK + (uint64_t)(((kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                   kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-          mma_ts_w(d + 64, tbase + COL_DOA + 8 * kk,
-                   bV + (uint64_t)(((kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+          mma_ts_w(d, a0 + 8 * kk,
+                   bB + (uint64_t)(((kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
                    kk > 0 ? 1u : 0u);
         mma_commit_w(smem_u32(&s.bar_s_full[bf]));
       }
       // this warp's MMAs must be complete before TMEM is freed (abort path)
-      mma_commit_w(smem_u32(&s.bar_x_done));
-      mbar_wait_warp(smem_u32(&s.bar_x_done), 0, wc, TAG_X_DONE);
+      mma_commit_w(smem_u32(&s.bar_x_done[is_s ? 0 : 1]));
+      mbar_wait_warp(smem_u32(&s.bar_x_done[is_s ? 0 : 1]), 0, wc, TAG_X_DONE);
     } else {
       // dQ += dS(n) K (A = dS packed in buffer n & 1, B = K tile, MN-major)
       bool ok = true;

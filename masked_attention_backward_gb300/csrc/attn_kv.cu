@@ -31,20 +31,20 @@
 // and 16 g + 8 (dS^T).  dS^T therefore does not occupy the dP^T buffer,
 // which is free again as soon as the softmax warps have read it.
 //
-// Two warps issue MMAs into the one tensor pipe: warp 1 the score products
-// S^T(m), dP^T(m), warp 2 the accumulations dV(n), dK(n).  The pipe accepts
-// only a few MMAs ahead of the one executing and a barrier wait costs a few
-// hundred cycles while the softmax warps keep the SM busy, so with a single
-// issuer every wait drained the pipe; with two, one warp's MMAs keep it fed
-// while the other waits.  S^T(m) waits for dK(m-2) (its buffer held
+// Three warps issue MMAs into the one tensor pipe: warp 1 S^T(m), warp 2
+// dP^T(m), warp 3 the accumulations dV(n), dK(n).  The pipe accepts only a
+// few MMAs ahead of the one executing and a barrier wait costs a few hundred
+// cycles while the softmax warps keep the SM busy, so with a single issuer
+// every wait drained the pipe; with several, one warp's MMAs keep it fed
+// while another waits.  S^T(m) waits for dK(m-2) (its buffer held
 // P^T / dS^T(m-2)), dP^T(m) for the softmax warps to have read dP^T(m-1),
 // dV(n) for P^T(n), dK(n) for dS^T(n).
 //
-// Warp roles (608 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues S^T / dP^T, warp 2 issues dV / dK (both whole warps, one elected
-// lane), warps 3..18 are the softmax warps: warp (sp, g) with sp = warp % 4
-// owns TMEM lanes 32 sp .. 32 sp + 31 (key rows) and query columns
-// 16 g .. 16 g + 15.
+// Warp roles (640 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues S^T, warp 2 issues dP^T, warp 3 issues dV / dK (whole warps, one
+// elected lane), warps 4..19 are the softmax warps: warp (sp, g) with
+// sp = warp % 4 owns TMEM lanes 32 sp .. 32 sp + 31 (key rows) and query
+// columns 16 g .. 16 g + 15.
 #include <math.h>
 
 #include "tiles.cuh"
@@ -60,7 +60,7 @@ constexpr int COL_KA = 256;    // K as the A operand (64 columns of 16-bit pairs
 constexpr int COL_ST = 320;    // S^T buffer b at COL_ST + 64 b
 constexpr int COL_DPT = 448;   // dP^T
 constexpr int SM_WARPS = 16;   // softmax warps
-constexpr int SM_WARP0 = 3;     // first softmax warp
+constexpr int SM_WARP0 = 4;     // first softmax warp
 constexpr int NUM_THREADS = 32 * (SM_WARP0 + SM_WARPS);
 
 struct __align__(1024) Smem {
@@ -79,7 +79,7 @@ struct __align__(1024) Smem {
   uint64_t bar_st_free[2];       // dV / dK MMAs that read the buffer complete
   uint64_t bar_dp_full;          // dP^T complete
   uint64_t bar_ds_full[2];       // step parity: dS^T packed, dP^T read (all softmax warps)
-  uint64_t bar_x_done;           // every S^T / dP^T MMA complete
+  uint64_t bar_x_done[2];        // every S^T (0) / dP^T (1) MMA complete
   uint64_t bar_acc_full;
   uint32_t tmem_base;
   int abort_flag;
@@ -137,7 +137,8 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     mbar_init(smem_u32(&s.bar_dp_full), 1);
     mbar_init(smem_u32(&s.bar_ds_full[0]), SM_WARPS);
     mbar_init(smem_u32(&s.bar_ds_full[1]), SM_WARPS);
-    mbar_init(smem_u32(&s.bar_x_done), 1);
+    mbar_init(smem_u32(&s.bar_x_done[0]), 1);
+    mbar_init(smem_u32(&s.bar_x_done[1]), 1);
     mbar_init(smem_u32(&s.bar_acc_full), 1);
     fence_mbar_init();
   }
@@ -189,16 +190,13 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         bulk_load(smem_u32(s.delta[st]), p.delta + srow, KV_SUB * 4, fb);
       }
     }
-  } else if (warp == 1 || warp == 2) {
+  } else if (warp >= 1 && warp < SM_WARP0) {
     // ------------------------------------------------------------ MMA issuers (whole warps)
     constexpr uint32_t ID_S = idesc_f16(BF16, KV_TILE, KV_SUB, false, false);
     constexpr uint32_t ID_ACC = idesc_f16(BF16, KV_TILE, HEAD_DIM, false, true);
     if (warp == 1) {
-      // S^T(m) = K Q^T into buffer m & 1 (A = K from TMEM, B = Q tile, K-major);
-      // dP^T(m) = V dO^T (A = V tile, B = dO tile, both K-major in shared memory)
-      const uint64_t aV = sdesc_sw128(smem_u32(s.V), 16, 1024);
-      bool ok = N == 0 || (mbar_wait_warp(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV) &&
-                           mbar_wait_warp(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA));
+      // S^T(m) = K Q^T into buffer m & 1 (A = K from TMEM, B = Q tile, K-major)
+      bool ok = N == 0 || mbar_wait_warp(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA);
       for (int m = 0; ok && m < N; ++m) {
         const int bf = m & 1, st = m % STAGES;
         ok = mbar_wait_warp(smem_u32(&s.bar_q_full[st]), (m / STAGES) & 1, wc, TAG_Q_FULL);
@@ -207,37 +205,42 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
           ok = mbar_wait_warp(smem_u32(&s.bar_st_free[bf]), ((m - 2) >> 1) & 1, wc, TAG_ST_FREE);
         if (!ok) break;
         tc_fence_after();
-        {
-          const uint32_t d = tbase + COL_ST + 64 * bf;
-          const uint64_t bQ = sdesc_sw128(smem_u32(stage_q(s, st)), 16, 1024);
+        const uint32_t d = tbase + COL_ST + 64 * bf;
+        const uint64_t bQ = sdesc_sw128(smem_u32(stage_q(s, st)), 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-            mma_ts_w(d, tbase + COL_KA + 8 * kk,
-                     bQ + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                     kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+          mma_ts_w(d, tbase + COL_KA + 8 * kk,
+                   bQ + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                   kk > 0 ? 1u : 0u);
         mma_commit_w(smem_u32(&s.bar_s_full[bf]));
-        // the softmax warps must have read dP^T(m - 1)
-        if (m >= 1) {
-          ok = mbar_wait_warp(smem_u32(&s.bar_ds_full[(m - 1) & 1]), ((m - 1) >> 1) & 1, wc,
-                              TAG_DS_FULL);
-          if (!ok) break;
-          tc_fence_after();
-        }
-        {
-          const uint64_t bO = sdesc_sw128(smem_u32(stage_do(s, st)), 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-            mma_ss_w(tbase + COL_DPT,
-                     aV + (uint64_t)(((kk >> 2) * (KV_TILE * 128) + (kk & 3) * 32) >> 4),
-                     bO + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                     kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(smem_u32(&s.bar_dp_full));
       }
       // this warp's MMAs must be complete before TMEM is freed (abort path)
-      mma_commit_w(smem_u32(&s.bar_x_done));
-      mbar_wait_warp(smem_u32(&s.bar_x_done), 0, wc, TAG_X_DONE);
+      mma_commit_w(smem_u32(&s.bar_x_done[0]));
+      mbar_wait_warp(smem_u32(&s.bar_x_done[0]), 0, wc, TAG_X_DONE);
+    } else if (warp == 2) {
+      // dP^T(m) = V dO^T (A = V tile, B = dO tile, both K-major in shared memory)
+      const uint64_t aV = sdesc_sw128(smem_u32(s.V), 16, 1024);
+      bool ok = N == 0 || mbar_wait_warp(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV);
+      for (int m = 0; ok && m < N; ++m) {
+        const int st = m % STAGES;
+        ok = mbar_wait_warp(smem_u32(&s.bar_q_full[st]), (m / STAGES) & 1, wc, TAG_Q_FULL);
+        // the softmax warps must have read dP^T(m - 1)
+        if (ok && m >= 1)
+          ok = mbar_wait_warp(smem_u32(&s.bar_ds_full[(m - 1) & 1]), ((m - 1) >> 1) & 1, wc,
+                              TAG_DS_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t bO = sdesc_sw128(smem_u32(stage_do(s, st)), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+          mma_ss_w(tbase + COL_DPT,
+                   aV + (uint64_t)(((kk >> 2) * (KV_TILE * 128) + (kk & 3) * 32) >> 4),
+                   bO + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                   kk > 0 ? 1u : 0u);
+        mma_commit_w(smem_u32(&s.bar_dp_full));
+      }
+      mma_commit_w(smem_u32(&s.bar_x_done[1]));
+      mbar_wait_warp(smem_u32(&s.bar_x_done[1]), 0, wc, TAG_X_DONE);
     } else {
       // dV += P^T(n) dO, dK += dS^T(n) Q (A from buffer n & 1, B MN-major)
       auto issue_acc = [&](int n, bool dkside) {
