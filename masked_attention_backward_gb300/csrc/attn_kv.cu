@@ -31,8 +31,8 @@
 // and 16 g + 8 (dS^T).  dS^T therefore does not occupy the dP^T buffer,
 // which is free again as soon as the softmax warps have read it.
 //
-// Three warps issue MMAs into the one tensor pipe: warp 1 S^T(m), warp 2
-// dP^T(m), warp 3 the accumulations dV(n), dK(n).  The pipe accepts only a
+// Four warps issue MMAs into the one tensor pipe: warp 1 S^T(m), warp 2
+// dP^T(m), warp 3 dV(n), warp 4 dK(n).  The pipe accepts only a
 // few MMAs ahead of the one executing and a barrier wait costs a few hundred
 // cycles while the softmax warps keep the SM busy, so with a single issuer
 // every wait drained the pipe; with several, one warp's MMAs keep it fed
@@ -40,9 +40,9 @@
 // P^T / dS^T(m-2)), dP^T(m) for the softmax warps to have read dP^T(m-1),
 // dV(n) for P^T(n), dK(n) for dS^T(n).
 //
-// Warp roles (640 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues S^T, warp 2 issues dP^T, warp 3 issues dV / dK (whole warps, one
-// elected lane), warps 4..19 are the softmax warps: warp (sp, g) with
+// Warp roles (672 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
+// issues S^T, warp 2 issues dP^T, warp 3 dV, warp 4 dK (whole warps, one
+// elected lane), warps 5..20 are the softmax warps: warp (sp, g) with
 // sp = warp % 4 owns TMEM lanes 32 sp .. 32 sp + 31 (key rows) and query
 // columns 16 g .. 16 g + 15.
 #include <math.h>
@@ -60,7 +60,7 @@ constexpr int COL_KA = 256;    // K as the A operand (64 columns of 16-bit pairs
 constexpr int COL_ST = 320;    // S^T buffer b at COL_ST + 64 b
 constexpr int COL_DPT = 448;   // dP^T
 constexpr int SM_WARPS = 16;   // softmax warps
-constexpr int SM_WARP0 = 4;     // first softmax warp
+constexpr int SM_WARP0 = 5;     // first softmax warp
 constexpr int NUM_THREADS = 32 * (SM_WARP0 + SM_WARPS);
 
 struct __align__(1024) Smem {
@@ -76,7 +76,7 @@ struct __align__(1024) Smem {
   uint64_t bar_q_empty[STAGES];
   uint64_t bar_s_full[2];        // S^T of the buffer complete
   uint64_t bar_p_full[2];        // P^T of the buffer packed (all softmax warps)
-  uint64_t bar_st_free[2];       // dV / dK MMAs that read the buffer complete
+  uint64_t bar_st_free[2];       // dV and dK MMAs that read the buffer complete (one commit each)
   uint64_t bar_dp_full;          // dP^T complete
   uint64_t bar_ds_full[2];       // step parity: dS^T packed, dP^T read (all softmax warps)
   uint64_t bar_x_done[2];        // every S^T (0) / dP^T (1) MMA complete
@@ -127,19 +127,19 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     mbar_init(smem_u32(&s.bar_ka_full), SM_WARPS);
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_u32(&s.bar_q_full[i]), 1);
-      mbar_init(smem_u32(&s.bar_q_empty[i]), 1);
+      mbar_init(smem_u32(&s.bar_q_empty[i]), 2);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_s_full[i]), 1);
       mbar_init(smem_u32(&s.bar_p_full[i]), SM_WARPS);
-      mbar_init(smem_u32(&s.bar_st_free[i]), 1);
+      mbar_init(smem_u32(&s.bar_st_free[i]), 2);
     }
     mbar_init(smem_u32(&s.bar_dp_full), 1);
     mbar_init(smem_u32(&s.bar_ds_full[0]), SM_WARPS);
     mbar_init(smem_u32(&s.bar_ds_full[1]), SM_WARPS);
     mbar_init(smem_u32(&s.bar_x_done[0]), 1);
     mbar_init(smem_u32(&s.bar_x_done[1]), 1);
-    mbar_init(smem_u32(&s.bar_acc_full), 1);
+    mbar_init(smem_u32(&s.bar_acc_full), 2);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -242,35 +242,32 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       mma_commit_w(smem_u32(&s.bar_x_done[1]));
       mbar_wait_warp(smem_u32(&s.bar_x_done[1]), 0, wc, TAG_X_DONE);
     } else {
-      // dV += P^T(n) dO, dK += dS^T(n) Q (A from buffer n & 1, B MN-major)
-      auto issue_acc = [&](int n, bool dkside) {
-        const uint32_t a = tbase + COL_ST + 64 * (n & 1) + (dkside ? 8 : 0);
-        const int st = n % STAGES;
+      // warp 3: dV += P^T(n) dO; warp 4: dK += dS^T(n) Q (A from buffer n & 1,
+      // B MN-major).  Each commits once to st_free, q_empty and acc_full,
+      // which complete on both commits.
+      const bool dkside = warp == 4;
+      const uint32_t acc = tbase + (dkside ? COL_DK : COL_DV);
+      bool ok = true;
+      for (int n = 0; ok && n < N; ++n) {
+        const int bf = n & 1, st = n % STAGES;
+        ok = dkside ? mbar_wait_warp(smem_u32(&s.bar_ds_full[bf]), (n >> 1) & 1, wc, TAG_DS_FULL)
+                    : mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), (n >> 1) & 1, wc, TAG_P_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t a = tbase + COL_ST + 64 * bf + (dkside ? 8 : 0);
         const uint64_t bB =
             sdesc_sw128(smem_u32(dkside ? stage_q(s, st) : stage_do(s, st)), KV_SUB * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < KV_SUB / 16; ++kk)
-          mma_ts_w(tbase + (dkside ? COL_DK : COL_DV), a + 16 * kk,
-                   bB + (uint64_t)((kk * 2048) >> 4), ID_ACC, (n > 0 || kk > 0) ? 1u : 0u);
-      };
-      bool ok = true;
-      for (int n = 0; ok && n < N; ++n) {
-        const int bf = n & 1;
-        ok = mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), (n >> 1) & 1, wc, TAG_P_FULL);
-        if (!ok) break;
-        tc_fence_after();
-        issue_acc(n, false);
-        ok = mbar_wait_warp(smem_u32(&s.bar_ds_full[bf]), (n >> 1) & 1, wc, TAG_DS_FULL);
-        if (!ok) break;
-        tc_fence_after();
-        issue_acc(n, true);
+          mma_ts_w(acc, a + 16 * kk, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC,
+                   (n > 0 || kk > 0) ? 1u : 0u);
         // S^T(n) and dP^T(n) completed before the softmax warps could signal
-        // step n, so this commit also frees the Q / dO stage
-        mma_commit_w(smem_u32(&s.bar_q_empty[n % STAGES]));
+        // step n, so these commits also free the Q / dO stage
+        mma_commit_w(smem_u32(&s.bar_q_empty[st]));
         mma_commit_w(smem_u32(&s.bar_st_free[bf]));
       }
-      // completes when every MMA issued above has (also on the abort path, so
-      // that TMEM is idle before it is freed)
+      // completes when every MMA of both warps has (also on the abort path,
+      // so that TMEM is idle before it is freed)
       mma_commit_w(smem_u32(&s.bar_acc_full));
       mbar_wait_warp(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
     }
