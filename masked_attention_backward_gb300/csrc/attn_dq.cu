@@ -62,6 +62,7 @@ struct __align__(1024) Smem {
   uint8_t dO[2 * Q_TILE * 128]; // later K/V stage 5
   uint8_t K[STAGES - 2][2 * Q_SUB * 128];
   uint8_t V[STAGES - 2][2 * Q_SUB * 128];
+  int step_t[STAGES];           // key sub-tile of the step in the stage
   uint64_t bar_q_full;          // Q, dO landed in shared memory
   uint64_t bar_qa_full;         // Q, dO copied into TMEM (all softmax warps)
   uint64_t bar_kv_full[STAGES];
@@ -162,6 +163,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         // warp has copied them into TMEM
         if (n == STAGES - 2 && !mbar_wait(smem_u32(&s.bar_qa_full), 0, wc, TAG_QA)) break;
         const int t = walk.tile(n);
+        s.step_t[st] = t;  // published by the arrive below together with the loads
         const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
         uint8_t* sk = stage_k(s, st);
         uint8_t* sv = stage_v(s, st);
@@ -268,20 +270,25 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
     const size_t srow = (size_t)bh * p.Sq_pad + i;
     const float lse2_i = p.lse2[srow];
     const float delta_i = p.delta[srow];
+    int flo, fhi;  // key sub-tiles that are entirely visible
+    full_range_q(p.mask_kind, p.window, p.Sq, p.Skv, q0, &flo, &fhi);
     for (int n = 0; ok && n < N; ++n) {
-      const int bf = n & 1;
-      if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (n >> 1) & 1, wc, TAG_S_FULL)) {
+      const int bf = n & 1, st = n % STAGES;
+      // s_full implies the stage's loads landed; waiting on kv_full as well
+      // makes the step's tile index (written by the producer) visible
+      if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (n >> 1) & 1, wc, TAG_S_FULL) ||
+          !mbar_wait(smem_u32(&s.bar_kv_full[st]), (n / STAGES) & 1, wc, TAG_KV_FULL)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int t = walk.tile(n);
       const uint32_t col = COL_BUF + bf * 128 + 16 * g;
       float sv[16], dp[16];
       tmem_ld16(lane_base + col, sv);
       tmem_ld16(lane_base + col + 64, dp);
+      const int t = s.step_t[st];
       // warp-uniform: the whole 128 x 64 sub-tile is visible
-      const bool full = tile_all_visible(p, q0, Q_TILE, t * Q_SUB, Q_SUB);
+      const bool full = t >= flo && t <= fhi;
       const uint32_t vis = full ? 0xffffu : vis_query_row(p, bh, i, t * Q_SUB + 16 * g);
       tmem_wait_ld_regs(sv);
 #pragma unroll

@@ -24,27 +24,26 @@
 // dS^T go back into TMEM and never touch shared memory.
 //
 // TMEM columns (512): dV [0,128), dK [128,256), K as 16-bit pairs [256,320),
-// two S^T buffers [320,384) and [384,448), dP^T [448,512).  Softmax group g
-// owns query columns 16 g .. 16 g + 15 of a sub-tile, i.e. 16 fp32 columns of
-// an S^T buffer; it packs P^T into the first 8 of them and dS^T into the
-// last 8, so the 16 queries of MMA K-step g sit at buffer column 16 g (P^T)
-// and 16 g + 8 (dS^T).  dS^T therefore does not occupy the dP^T buffer,
-// which is free again as soon as the softmax warps have read it.
+// S^T [320,384), dP^T [384,448), packed P^T [448,480), packed dS^T
+// [480,512).  Softmax group g owns query columns 16 g .. 16 g + 15 of a
+// sub-tile, so the 16 queries of MMA K-step g sit at column 8 g of the packed
+// regions.  Because P^T and dS^T have regions of their own, the fp32 S^T and
+// dP^T buffers are free as soon as the softmax warps have loaded them into
+// registers: S^T(n+1) runs while the softmax warps turn S^T(n) into P^T(n),
+// and dP^T(n+1) while they turn dP^T(n) into dS^T(n).  Only the packed
+// regions wait for the accumulations: P^T(n+1) is written once dV(n) has
+// read P^T(n), dS^T(n+1) once dK(n) has read dS^T(n).
 //
-// Four warps issue MMAs into the one tensor pipe: warp 1 S^T(m), warp 2
-// dP^T(m), warp 3 dV(n), warp 4 dK(n).  The pipe accepts only a
-// few MMAs ahead of the one executing and a barrier wait costs a few hundred
-// cycles while the softmax warps keep the SM busy, so with a single issuer
-// every wait drained the pipe; with several, one warp's MMAs keep it fed
-// while another waits.  S^T(m) waits for dK(m-2) (its buffer held
-// P^T / dS^T(m-2)), dP^T(m) for the softmax warps to have read dP^T(m-1),
-// dV(n) for P^T(n), dK(n) for dS^T(n).
+// Four warps issue MMAs into the one tensor pipe, each waiting only on its own
+// inputs: warp 1 S^T(m), warp 2 dP^T(m), warp 3 dV(n), warp 4 dK(n).  The pipe
+// accepts only a few MMAs ahead of the one executing and a barrier wait costs
+// a few hundred cycles while the softmax warps keep the SM busy, so one
+// issuing warp would drain the pipe at every wait.
 //
-// Warp roles (672 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
-// issues S^T, warp 2 issues dP^T, warp 3 dV, warp 4 dK (whole warps, one
-// elected lane), warps 5..20 are the softmax warps: warp (sp, g) with
-// sp = warp % 4 owns TMEM lanes 32 sp .. 32 sp + 31 (key rows) and query
-// columns 16 g .. 16 g + 15.
+// Warp roles (672 threads): warp 0 issues TMA loads, warp 1 owns TMEM; warps
+// 1..4 issue MMAs (whole warps, one elected lane); warps 5..20 are the
+// softmax warps: warp (sp, g) with sp = warp % 4 owns TMEM lanes
+// 32 sp .. 32 sp + 31 (key rows) and query columns 16 g .. 16 g + 15.
 #include <math.h>
 
 #include "tiles.cuh"
@@ -57,8 +56,10 @@ constexpr int STAGES = 5;      // Q/dO ring depth; the last stage reuses K's til
 constexpr int COL_DV = 0;
 constexpr int COL_DK = 128;
 constexpr int COL_KA = 256;    // K as the A operand (64 columns of 16-bit pairs)
-constexpr int COL_ST = 320;    // S^T buffer b at COL_ST + 64 b
-constexpr int COL_DPT = 448;   // dP^T
+constexpr int COL_ST = 320;    // S^T, fp32
+constexpr int COL_DPT = 384;   // dP^T, fp32
+constexpr int COL_PT = 448;    // P^T, 16-bit pairs
+constexpr int COL_DST = 480;   // dS^T, 16-bit pairs
 constexpr int SM_WARPS = 16;   // softmax warps
 constexpr int SM_WARP0 = 5;     // first softmax warp
 constexpr int NUM_THREADS = 32 * (SM_WARP0 + SM_WARPS);
@@ -70,17 +71,22 @@ struct __align__(1024) Smem {
   uint8_t dO[STAGES - 1][2 * KV_SUB * 128];
   float lse2[STAGES][KV_SUB];
   float delta[STAGES][KV_SUB];
+  int step_r[STAGES];            // query sub-tile of the step in the stage
+  int step_hh[STAGES];           // its query head within the group
   uint64_t bar_kv_full;          // K, V landed
   uint64_t bar_ka_full;          // K copied into TMEM (all softmax warps)
   uint64_t bar_q_full[STAGES];
-  uint64_t bar_q_empty[STAGES];
-  uint64_t bar_s_full[2];        // S^T of the buffer complete
-  uint64_t bar_p_full[2];        // P^T of the buffer packed (all softmax warps)
-  uint64_t bar_st_free[2];       // dV and dK MMAs that read the buffer complete (one commit each)
+  uint64_t bar_q_empty[STAGES];  // dV and dK of the step complete (one commit each)
+  uint64_t bar_s_full;           // S^T complete
+  uint64_t bar_s_free;           // S^T loaded by every softmax warp
   uint64_t bar_dp_full;          // dP^T complete
-  uint64_t bar_ds_full[2];       // step parity: dS^T packed, dP^T read (all softmax warps)
+  uint64_t bar_dp_free;          // dP^T loaded by every softmax warp
+  uint64_t bar_p_full;           // P^T written by every softmax warp
+  uint64_t bar_pt_free;          // dV that read P^T complete
+  uint64_t bar_ds_full;          // dS^T written by every softmax warp
+  uint64_t bar_dst_free;         // dK that read dS^T complete
   uint64_t bar_x_done[2];        // every S^T (0) / dP^T (1) MMA complete
-  uint64_t bar_acc_full;
+  uint64_t bar_acc_full;         // every dV and dK MMA complete (one commit each)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -96,8 +102,8 @@ __device__ __forceinline__ uint8_t* stage_do(Smem& s, int st) {
   return st < STAGES - 1 ? s.dO[st] : s.K + 2 * KV_SUB * 128;
 }
 
-enum { TAG_KV = 0x201, TAG_KA, TAG_Q_EMPTY, TAG_Q_FULL, TAG_ST_FREE, TAG_P_FULL, TAG_S_FULL,
-       TAG_DP_FULL, TAG_DS_FULL, TAG_ACC, TAG_X_DONE };
+enum { TAG_KV = 0x201, TAG_KA, TAG_Q_EMPTY, TAG_Q_FULL, TAG_S_FREE, TAG_P_FULL, TAG_S_FULL,
+       TAG_DP_FULL, TAG_DS_FULL, TAG_ACC, TAG_X_DONE, TAG_DP_FREE, TAG_PT_FREE, TAG_DST_FREE };
 
 }  // namespace kv_side
 
@@ -129,14 +135,14 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       mbar_init(smem_u32(&s.bar_q_full[i]), 1);
       mbar_init(smem_u32(&s.bar_q_empty[i]), 2);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&s.bar_s_full[i]), 1);
-      mbar_init(smem_u32(&s.bar_p_full[i]), SM_WARPS);
-      mbar_init(smem_u32(&s.bar_st_free[i]), 2);
-    }
+    mbar_init(smem_u32(&s.bar_s_full), 1);
+    mbar_init(smem_u32(&s.bar_s_free), SM_WARPS);
     mbar_init(smem_u32(&s.bar_dp_full), 1);
-    mbar_init(smem_u32(&s.bar_ds_full[0]), SM_WARPS);
-    mbar_init(smem_u32(&s.bar_ds_full[1]), SM_WARPS);
+    mbar_init(smem_u32(&s.bar_dp_free), SM_WARPS);
+    mbar_init(smem_u32(&s.bar_p_full), SM_WARPS);
+    mbar_init(smem_u32(&s.bar_pt_free), 1);
+    mbar_init(smem_u32(&s.bar_ds_full), SM_WARPS);
+    mbar_init(smem_u32(&s.bar_dst_free), 1);
     mbar_init(smem_u32(&s.bar_x_done[0]), 1);
     mbar_init(smem_u32(&s.bar_x_done[1]), 1);
     mbar_init(smem_u32(&s.bar_acc_full), 2);
@@ -176,6 +182,10 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         if (n == STAGES - 1 && !mbar_wait(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA)) break;
         const int r = walk.tile(p, cur.hh, cur.idx);
         const int bh = b * p.Hq + c * p.group + cur.hh;
+        // the step's coordinates for the softmax warps, published by the
+        // arrive below together with the loads
+        s.step_r[st] = r;
+        s.step_hh[st] = cur.hh;
         cur.next(p, walk);
         const uint32_t fb = smem_u32(&s.bar_q_full[st]);
         mbar_arrive_expect_tx(fb, 4 * KV_SUB * 128 + 2 * KV_SUB * 4);
@@ -194,77 +204,71 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     // ------------------------------------------------------------ MMA issuers (whole warps)
     constexpr uint32_t ID_S = idesc_f16(BF16, KV_TILE, KV_SUB, false, false);
     constexpr uint32_t ID_ACC = idesc_f16(BF16, KV_TILE, HEAD_DIM, false, true);
-    if (warp == 1) {
-      // S^T(m) = K Q^T into buffer m & 1 (A = K from TMEM, B = Q tile, K-major)
-      bool ok = N == 0 || mbar_wait_warp(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA);
-      for (int m = 0; ok && m < N; ++m) {
-        const int bf = m & 1, st = m % STAGES;
-        ok = mbar_wait_warp(smem_u32(&s.bar_q_full[st]), (m / STAGES) & 1, wc, TAG_Q_FULL);
-        // the buffer held P^T / dS^T(m - 2): dV(m - 2) and dK(m - 2) must be done
-        if (ok && m >= 2)
-          ok = mbar_wait_warp(smem_u32(&s.bar_st_free[bf]), ((m - 2) >> 1) & 1, wc, TAG_ST_FREE);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d = tbase + COL_ST + 64 * bf;
-        const uint64_t bQ = sdesc_sw128(smem_u32(stage_q(s, st)), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-          mma_ts_w(d, tbase + COL_KA + 8 * kk,
-                   bQ + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                   kk > 0 ? 1u : 0u);
-        mma_commit_w(smem_u32(&s.bar_s_full[bf]));
-      }
-      // this warp's MMAs must be complete before TMEM is freed (abort path)
-      mma_commit_w(smem_u32(&s.bar_x_done[0]));
-      mbar_wait_warp(smem_u32(&s.bar_x_done[0]), 0, wc, TAG_X_DONE);
-    } else if (warp == 2) {
-      // dP^T(m) = V dO^T (A = V tile, B = dO tile, both K-major in shared memory)
+    if (warp == 1 || warp == 2) {
+      // warp 1: S^T(m) = K Q^T (A = K from TMEM, B = Q tile, K-major);
+      // warp 2: dP^T(m) = V dO^T (A = V tile, B = dO tile, both K-major in
+      // shared memory).  Each waits for the softmax warps to have loaded its
+      // previous result.
+      const bool is_s = warp == 1;
+      const uint32_t free_bar = smem_u32(is_s ? &s.bar_s_free : &s.bar_dp_free);
+      const uint32_t full_bar = smem_u32(is_s ? &s.bar_s_full : &s.bar_dp_full);
       const uint64_t aV = sdesc_sw128(smem_u32(s.V), 16, 1024);
-      bool ok = N == 0 || mbar_wait_warp(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV);
+      bool ok = N == 0 || (is_s ? mbar_wait_warp(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA)
+                                : mbar_wait_warp(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV));
       for (int m = 0; ok && m < N; ++m) {
         const int st = m % STAGES;
         ok = mbar_wait_warp(smem_u32(&s.bar_q_full[st]), (m / STAGES) & 1, wc, TAG_Q_FULL);
-        // the softmax warps must have read dP^T(m - 1)
         if (ok && m >= 1)
-          ok = mbar_wait_warp(smem_u32(&s.bar_ds_full[(m - 1) & 1]), ((m - 1) >> 1) & 1, wc,
-                              TAG_DS_FULL);
+          ok = mbar_wait_warp(free_bar, (m - 1) & 1, wc, is_s ? TAG_S_FREE : TAG_DP_FREE);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t bO = sdesc_sw128(smem_u32(stage_do(s, st)), 16, 1024);
+        if (is_s) {
+          const uint64_t bQ = sdesc_sw128(smem_u32(stage_q(s, st)), 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-          mma_ss_w(tbase + COL_DPT,
-                   aV + (uint64_t)(((kk >> 2) * (KV_TILE * 128) + (kk & 3) * 32) >> 4),
-                   bO + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                   kk > 0 ? 1u : 0u);
-        mma_commit_w(smem_u32(&s.bar_dp_full));
+          for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+            mma_ts_w(tbase + COL_ST, tbase + COL_KA + 8 * kk,
+                     bQ + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                     kk > 0 ? 1u : 0u);
+        } else {
+          const uint64_t bO = sdesc_sw128(smem_u32(stage_do(s, st)), 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+            mma_ss_w(tbase + COL_DPT,
+                     aV + (uint64_t)(((kk >> 2) * (KV_TILE * 128) + (kk & 3) * 32) >> 4),
+                     bO + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                     kk > 0 ? 1u : 0u);
+        }
+        mma_commit_w(full_bar);
       }
-      mma_commit_w(smem_u32(&s.bar_x_done[1]));
-      mbar_wait_warp(smem_u32(&s.bar_x_done[1]), 0, wc, TAG_X_DONE);
+      // this warp's MMAs must be complete before TMEM is freed (abort path)
+      const uint32_t done = smem_u32(&s.bar_x_done[is_s ? 0 : 1]);
+      mma_commit_w(done);
+      mbar_wait_warp(done, 0, wc, TAG_X_DONE);
     } else {
-      // warp 3: dV += P^T(n) dO; warp 4: dK += dS^T(n) Q (A from buffer n & 1,
-      // B MN-major).  Each commits once to st_free, q_empty and acc_full,
-      // which complete on both commits.
+      // warp 3: dV += P^T(n) dO; warp 4: dK += dS^T(n) Q (A from the packed
+      // regions, B MN-major).  Both commit to q_empty and acc_full, which
+      // complete on the two commits.
       const bool dkside = warp == 4;
       const uint32_t acc = tbase + (dkside ? COL_DK : COL_DV);
+      const uint32_t a = tbase + (dkside ? COL_DST : COL_PT);
+      const uint32_t full_bar = smem_u32(dkside ? &s.bar_ds_full : &s.bar_p_full);
+      const uint32_t free_bar = smem_u32(dkside ? &s.bar_dst_free : &s.bar_pt_free);
       bool ok = true;
       for (int n = 0; ok && n < N; ++n) {
-        const int bf = n & 1, st = n % STAGES;
-        ok = dkside ? mbar_wait_warp(smem_u32(&s.bar_ds_full[bf]), (n >> 1) & 1, wc, TAG_DS_FULL)
-                    : mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), (n >> 1) & 1, wc, TAG_P_FULL);
+        const int st = n % STAGES;
+        ok = mbar_wait_warp(full_bar, n & 1, wc, dkside ? TAG_DS_FULL : TAG_P_FULL);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t a = tbase + COL_ST + 64 * bf + (dkside ? 8 : 0);
         const uint64_t bB =
             sdesc_sw128(smem_u32(dkside ? stage_q(s, st) : stage_do(s, st)), KV_SUB * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < KV_SUB / 16; ++kk)
-          mma_ts_w(acc, a + 16 * kk, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC,
+          mma_ts_w(acc, a + 8 * kk, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC,
                    (n > 0 || kk > 0) ? 1u : 0u);
-        // S^T(n) and dP^T(n) completed before the softmax warps could signal
-        // step n, so these commits also free the Q / dO stage
+        mma_commit_w(free_bar);
+        // S^T(n) and dP^T(n) completed before the softmax warps could write
+        // P^T(n) / dS^T(n), so the two commits also free the Q / dO stage
         mma_commit_w(smem_u32(&s.bar_q_empty[st]));
-        mma_commit_w(smem_u32(&s.bar_st_free[bf]));
       }
       // completes when every MMA of both warps has (also on the abort path,
       // so that TMEM is idle before it is freed)
@@ -299,27 +303,33 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&s.bar_ka_full));
 
-    KVCursor cur;
-    cur.start(p, walk);
+    // signal one barrier from this warp once its TMEM accesses are done
+    auto warp_arrive = [&](uint64_t* bar) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(bar));
+    };
+    int flo, fhi;  // query sub-tiles that are entirely visible
+    full_range_kv(p.mask_kind, p.window, p.Sq, p.Skv, k0, &flo, &fhi);
     for (int n = 0; ok && n < N; ++n) {
-      const int bf = n & 1, st = n % STAGES;
-      const uint32_t col = COL_ST + 64 * bf + 16 * g;
+      const int st = n % STAGES;
+      // ---- P^T(n) = exp2(S^T(n) * scale*log2e - lse2)
       // s_full implies the stage's loads landed; waiting on q_full as well
       // makes the bulk-copied lse2 / Delta rows visible to this thread
-      if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (n >> 1) & 1, wc, TAG_S_FULL) ||
+      if (!mbar_wait(smem_u32(&s.bar_s_full), n & 1, wc, TAG_S_FULL) ||
           !mbar_wait(smem_u32(&s.bar_q_full[st]), (n / STAGES) & 1, wc, TAG_Q_FULL)) {
         ok = false;
         break;
       }
       tc_fence_after();
       float sv[16];
-      tmem_ld16(lane_base + col, sv);
-      const int r = walk.tile(p, cur.hh, cur.idx);
-      const int bh = b * p.Hq + c * p.group + cur.hh;
-      cur.next(p, walk);
+      tmem_ld16(lane_base + COL_ST + 16 * g, sv);
+      const int r = s.step_r[st];
       // warp-uniform: the whole 64 x 128 sub-tile is visible
-      const bool full = tile_all_visible(p, r * KV_SUB, KV_SUB, k0, KV_TILE);
-      const uint32_t vis = full ? 0xffffu : vis_key_row(p, bh, j, r * KV_SUB + 16 * g);
+      const bool full = r >= flo && r <= fhi;
+      const uint32_t vis =
+          full ? 0xffffu
+               : vis_key_row(p, b * p.Hq + c * p.group + s.step_hh[st], j, r * KV_SUB + 16 * g);
       const float4* l4 = reinterpret_cast<const float4*>(&s.lse2[st][16 * g]);
       float lv[16];
 #pragma unroll
@@ -331,6 +341,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         lv[4 * q + 3] = L.w;
       }
       tmem_wait_ld_regs(sv);
+      warp_arrive(&s.bar_s_free);  // S^T(n + 1) may overwrite the buffer
       float pv[16];
       uint32_t pk[8];
       if (full) {
@@ -345,12 +356,17 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       }
 #pragma unroll
       for (int q = 0; q < 8; ++q) pk[q] = pack2<BF16>(pv[2 * q], pv[2 * q + 1]);
-      tmem_st8(lane_base + col, pk);
+      // dV(n - 1) must have read P^T(n - 1)
+      if (n >= 1 && !mbar_wait(smem_u32(&s.bar_pt_free), (n - 1) & 1, wc, TAG_PT_FREE)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st8(lane_base + COL_PT + 8 * g, pk);
       tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s.bar_p_full[bf]));
+      warp_arrive(&s.bar_p_full);
 
+      // ---- dS^T(n) = P^T(n) (dP^T(n) - Delta)
       const float4* d4 = reinterpret_cast<const float4*>(&s.delta[st][16 * g]);
       float dl[16];
 #pragma unroll
@@ -369,15 +385,20 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       float dp[16];
       tmem_ld16(lane_base + COL_DPT + 16 * g, dp);
       tmem_wait_ld_regs(dp);
+      warp_arrive(&s.bar_dp_free);  // dP^T(n + 1) may overwrite the buffer
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         pk[q] = pack2<BF16>(pv[2 * q] * (dp[2 * q] - dl[2 * q]),
                             pv[2 * q + 1] * (dp[2 * q + 1] - dl[2 * q + 1]));
-      tmem_st8(lane_base + col + 8, pk);
+      // dK(n - 1) must have read dS^T(n - 1)
+      if (n >= 1 && !mbar_wait(smem_u32(&s.bar_dst_free), (n - 1) & 1, wc, TAG_DST_FREE)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st8(lane_base + COL_DST + 8 * g, pk);
       tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s.bar_ds_full[bf]));
+      warp_arrive(&s.bar_ds_full);
     }
     // ---------------------------------------------------------- epilogue
     bool have = ok && N > 0;

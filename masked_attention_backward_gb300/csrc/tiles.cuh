@@ -81,6 +81,50 @@ __device__ __forceinline__ bool tile_all_visible(const AttnParams& p, int i0, in
   }
 }
 
+// The sub-tiles of a walk that are entirely visible form one contiguous
+// range [lo, hi] of partner tile indices under the closed-form masks (empty,
+// hi < lo, for block masks, whose tiles always take the per-element path).
+// Computed once per CTA, so that a step decides with two compares.
+//
+// Key-tile CTA [k0, k0 + KV_TILE) against query sub-tiles r of KV_SUB rows:
+// every (i, j) with i in [r KV_SUB, r KV_SUB + KV_SUB), j in [k0, k0 + KV_TILE)
+// must exist (i < Sq, j < Skv) and, causal / sliding, satisfy j <= i
+// (r KV_SUB >= k0 + KV_TILE - 1) and, sliding, i - j < window
+// (r KV_SUB + KV_SUB - 1 - k0 <= window - 1).
+__host__ __device__ inline void full_range_kv(int kind, int window, int Sq, int Skv, int k0,
+                                              int* lo, int* hi) {
+  *lo = 0;
+  *hi = Sq / KV_SUB - 1;  // r KV_SUB + KV_SUB <= Sq
+  if (kind == MK_BLOCK || k0 + KV_TILE > Skv) *hi = -1;
+  if (kind == MK_CAUSAL || kind == MK_SLIDING) *lo = (k0 + KV_TILE - 1 + KV_SUB - 1) / KV_SUB;
+  if (kind == MK_SLIDING) {
+    const int top = window + k0 - KV_SUB;  // r KV_SUB <= top
+    const int h = top < 0 ? -1 : top / KV_SUB;
+    if (h < *hi) *hi = h;
+  }
+}
+
+// Query-tile CTA [q0, q0 + Q_TILE) against key sub-tiles t of Q_SUB rows:
+// every i in [q0, q0 + Q_TILE), j in [t Q_SUB, t Q_SUB + Q_SUB) must exist
+// and, causal / sliding, satisfy j <= i (t Q_SUB + Q_SUB - 1 <= q0) and,
+// sliding, i - j < window (q0 + Q_TILE - 1 - t Q_SUB <= window - 1).
+__host__ __device__ inline void full_range_q(int kind, int window, int Sq, int Skv, int q0,
+                                             int* lo, int* hi) {
+  *lo = 0;
+  *hi = Skv / Q_SUB - 1;  // t Q_SUB + Q_SUB <= Skv
+  if (kind == MK_BLOCK || q0 + Q_TILE > Sq) *hi = -1;
+  if (kind == MK_CAUSAL || kind == MK_SLIDING) {
+    const int top = q0 - (Q_SUB - 1);  // t Q_SUB <= top
+    const int h = top < 0 ? -1 : top / Q_SUB;
+    if (h < *hi) *hi = h;
+  }
+  if (kind == MK_SLIDING) {
+    const int bot = q0 + Q_TILE - window;  // t Q_SUB >= bot
+    const int l = bot <= 0 ? 0 : (bot + Q_SUB - 1) / Q_SUB;
+    if (l > *lo) *lo = l;
+  }
+}
+
 // Walk of a query-tile CTA (Q_TILE rows of head bh) over key sub-tiles of
 // Q_SUB rows.
 struct QWalk {
