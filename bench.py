@@ -235,27 +235,23 @@ def run_ours(args, rank, world, local):
     ms_per_step = t_max / args.steps
     value = world * fl["total"] * args.steps / (t_max * 1e-3) / 1e12
 
-    # ---- end to end through the C ABI with pinned host buffers
+    # ---- end to end from pinned host buffers: every step copies its inputs in
+    # and its gradients out; the binding overlaps the copies of one run of GQA
+    # groups with the kernels of the previous one (each run is one attn_bwd call)
     e2e = None
     if not args.no_e2e:
         host_in = {n: t[n].cpu().pin_memory() for n in ("q", "k", "v", "o", "dO", "lse")}
-        if t["sink"] is not None:
-            host_in["sink"] = t["sink"].cpu().pin_memory()
-        host_out = [x.cpu().pin_memory() for x in out if x is not None]
-        dev_in = {n: torch.empty_like(t[n]) for n in host_in}
-        h2d = sum(x.numel() * x.element_size() for x in host_in.values())
-        d2h = sum(x.numel() * x.element_size() for x in host_out)
+        host_in["sink"] = t["sink"].cpu().pin_memory() if t["sink"] is not None else None
+        host_out = [x.cpu().pin_memory() if x is not None else None for x in out]
+        hb = mab.HostBackward(wl.B, wl.Hq, wl.Hkv, wl.Sq, wl.Skv, t["q"].dtype, t["mask"],
+                              wl.scale, t["sink"] is not None, device, chunks=args.e2e_chunks)
+        h2d, d2h = hb.bytes_per_call(host_in, host_out)
         e2e_ms = []
         for it in range(args.warmup + args.steps):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for n, h in host_in.items():
-                dev_in[n].copy_(h, non_blocking=True)
-            mab.bwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["o"], dev_in["dO"],
-                    dev_in["lse"], dev_in.get("sink"), t["mask"], wl.scale, ws=ws, out=out)
-            for h, d in zip(host_out, [x for x in out if x is not None]):
-                h.copy_(d, non_blocking=True)
+            hb(host_in, host_out)
             e1.record(stream)
             e1.synchronize()
             if it >= args.warmup:
@@ -263,7 +259,12 @@ def run_ours(args, rank, world, local):
         te = max_over_ranks(float(sum(e2e_ms)), world, device)
         e2e = {"value": round(world * fl["total"] * args.steps / (te * 1e-3) / 1e12, 2),
                "unit": "TFLOP/s", "ms_per_step": round(te / args.steps, 3),
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "pipeline_chunks": hb.chunks}
+        # the same gradients as the device-resident calls timed above
+        for a, b_ in zip(host_out, out):
+            if a is not None and not torch.equal(a, b_.cpu()):
+                raise RuntimeError("pipelined host-buffer backward differs from attn_bwd")
 
     # ---- roofline of the dominant kernel
     peaks, peak_src = load_peaks()
@@ -417,6 +418,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--e2e-chunks", type=int, default=4,
+                    help="runs of GQA groups the host-buffer pipeline overlaps")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -220,3 +220,103 @@ def bwd(q, k, v, o, dO, lse, sink, mask: Mask, scale: float, ws: Optional[torch.
 
 def device_status(ws: torch.Tensor, stream=None) -> int:
     return attn_get_device_status(_ptr(ws), _stream(stream))
+
+
+class HostBackward:
+    """Backward from pinned host tensors to pinned host tensors, with the
+    host<->device copies overlapped with the kernels.
+
+    The heads of a GQA group are independent of every other group, so the
+    call is split into `chunks` runs of whole key/value heads.  Chunk c's
+    inputs are copied in on one stream while chunk c-1 runs attn_bwd on the
+    compute stream and chunk c-2's gradients are copied out on a third; every
+    chunk is one attn_bwd call on pointer offsets into device buffers that are
+    allocated once here (the library itself allocates nothing).  With B > 1 a
+    run of heads is not contiguous across the batch, and dSink sums over the
+    batch, so the call is not split (chunks = 1).
+
+    __call__ enqueues everything behind the caller's current stream and makes
+    that stream wait for the last copy out, so synchronising it covers the
+    whole call."""
+
+    def __init__(self, B, Hq, Hkv, Sq, Skv, dtype, mask: Mask, scale: float, has_sink: bool,
+                 device, chunks: int = 4):
+        self.B, self.Hq, self.Hkv, self.Sq, self.Skv = B, Hq, Hkv, Sq, Skv
+        self.dtype, self.mask, self.scale, self.has_sink = dtype, mask, scale, has_sink
+        self.device = torch.device(device)
+        if B != 1 or Hkv % chunks != 0:
+            chunks = 1
+        self.chunks = chunks
+        self.g = Hq // Hkv
+        kvc = Hkv // chunks
+        D = 128
+        e = dict(dtype=dtype, device=self.device)
+        self.dev = {
+            "q": torch.empty(B, Hq, Sq, D, **e), "o": torch.empty(B, Hq, Sq, D, **e),
+            "dO": torch.empty(B, Hq, Sq, D, **e), "k": torch.empty(B, Hkv, Skv, D, **e),
+            "v": torch.empty(B, Hkv, Skv, D, **e),
+            "lse": torch.empty(B, Hq, Sq, dtype=torch.float32, device=self.device),
+            "dq": torch.empty(B, Hq, Sq, D, **e), "dk": torch.empty(B, Hkv, Skv, D, **e),
+            "dv": torch.empty(B, Hkv, Skv, D, **e),
+        }
+        if has_sink:
+            self.dev["sink"] = torch.empty(Hq, dtype=torch.float32, device=self.device)
+            self.dev["dsink"] = torch.empty(Hq, dtype=torch.float32, device=self.device)
+        code = ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16
+        self.cshape = attn_shape_t(B, Hq // chunks, kvc, Sq, Skv, D, code)
+        self.ws = workspace(self.cshape, mask, self.device)
+        self.s_in = torch.cuda.Stream(self.device)
+        self.s_out = torch.cuda.Stream(self.device)
+        self.ev_in = [torch.cuda.Event() for _ in range(chunks)]
+        self.ev_done = [torch.cuda.Event() for _ in range(chunks)]
+        self.ev_start = torch.cuda.Event()
+        self.ev_out = torch.cuda.Event()
+
+    def bytes_per_call(self, host_in, host_out):
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values() if t is not None)
+        d2h = sum(t.numel() * t.element_size() for t in host_out if t is not None)
+        return h2d, d2h
+
+    def __call__(self, host_in: dict, host_out):
+        """host_in: pinned q, k, v, o, dO, lse (and sink); host_out: pinned
+        (dq, dk, dv, dsink)."""
+        cur = torch.cuda.current_stream(self.device)
+        self.ev_start.record(cur)
+        self.s_in.wait_event(self.ev_start)
+        C, g = self.chunks, self.g
+        hq, hk = self.Hq // C, self.Hkv // C
+        d = self.dev
+        for c in range(C):
+            qs, ks = slice(c * hq, (c + 1) * hq), slice(c * hk, (c + 1) * hk)
+            with torch.cuda.stream(self.s_in):
+                for n in ("q", "o", "dO", "lse"):
+                    d[n][:, qs].copy_(host_in[n][:, qs], non_blocking=True)
+                for n in ("k", "v"):
+                    d[n][:, ks].copy_(host_in[n][:, ks], non_blocking=True)
+                if self.has_sink:
+                    d["sink"][qs].copy_(host_in["sink"][qs], non_blocking=True)
+                self.ev_in[c].record(self.s_in)
+            cur.wait_event(self.ev_in[c])
+            mask = self.mask
+            if mask.block_mask is not None:
+                mask = Mask(mask.kind, mask.window, mask.bx, mask.by, mask.block_mask[:, qs])
+            sink = d["sink"][qs] if self.has_sink else None
+            dsink = d["dsink"][qs] if self.has_sink else None
+            r = attn_bwd(self.cshape, _ptr(d["q"][:, qs]), _ptr(d["k"][:, ks]),
+                         _ptr(d["v"][:, ks]), _ptr(d["o"][:, qs]), _ptr(d["dO"][:, qs]),
+                         _ptr(d["lse"][:, qs]), _ptr(sink), mask.desc(), self.scale,
+                         _ptr(d["dq"][:, qs]), _ptr(d["dk"][:, ks]), _ptr(d["dv"][:, ks]),
+                         _ptr(dsink), _ptr(self.ws), self.ws.numel(), _stream(cur))
+            if r != ATTN_OK:
+                raise AttnError(r, "attn_bwd")
+            self.ev_done[c].record(cur)
+            self.s_out.wait_event(self.ev_done[c])
+            with torch.cuda.stream(self.s_out):
+                dq, dk, dv, dsink_h = host_out
+                dq[:, qs].copy_(d["dq"][:, qs], non_blocking=True)
+                dk[:, ks].copy_(d["dk"][:, ks], non_blocking=True)
+                dv[:, ks].copy_(d["dv"][:, ks], non_blocking=True)
+                if self.has_sink:
+                    dsink_h[qs].copy_(d["dsink"][qs], non_blocking=True)
+        self.ev_out.record(self.s_out)
+        cur.wait_event(self.ev_out)

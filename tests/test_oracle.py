@@ -151,10 +151,13 @@ def test_against_torch_sdpa(kind, with_sink):
     dO = _rand(rng, B, Hq, S, D)
     ours = oracle.backward_exact(pb, q, k, v, dO)
     ref = _sdpa_reference(pb, q, k, v, dO)
+    # torch's fp64 attention on the CPU reaches its result in a different
+    # order from run to run (seen: 2e-10 relative on LSE within a full test
+    # session); 1e-8 relative still fails any wrong term, sign or index
     for name in ("o", "lse", "dq", "dk", "dv"):
-        np.testing.assert_allclose(ours[name], ref[name], rtol=1e-10, atol=1e-11, err_msg=name)
+        np.testing.assert_allclose(ours[name], ref[name], rtol=1e-8, atol=1e-9, err_msg=name)
     if with_sink:
-        np.testing.assert_allclose(ours["dsink"], ref["dsink"], rtol=1e-10, atol=1e-11)
+        np.testing.assert_allclose(ours["dsink"], ref["dsink"], rtol=1e-8, atol=1e-9)
     else:
         assert np.all(ours["dsink"] == 0)
 
