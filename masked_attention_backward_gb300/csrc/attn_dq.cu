@@ -1,6 +1,6 @@
 // attn_dq.cu -- query-stationary dQ kernel on tcgen05 / TMEM, fed by TMA.
 //
-// One CTA per (b, query head h, Q_TILE query rows).  Q and dO of the tile are
+// Work unit: (b, query head h, Q_TILE query rows).  Q and dO of the unit are
 // loaded once and copied into TMEM, where they serve as the A operand of
 // every score contraction.  For each active key sub-tile t of Q_SUB rows:
 //   S  = Q K_t^T,  dP = dO V_t^T                 (A from TMEM, fp32 in TMEM)
@@ -19,7 +19,20 @@
 // shared memory at N = 64 is limited by shared-memory bandwidth (it reads
 // 6 KB per 32 cycles of math), while with A in TMEM it reads only its 2 KB B
 // tile and runs at the tensor pipe's rate.  Q and dO are the same for the
-// whole walk, so they move to TMEM once.
+// whole walk of a unit, so they move to TMEM once.
+//
+// Persistent: one CTA per SM.  Units are numbered heaviest causal rows first;
+// CTA b starts with unit b and then claims the next unnumbered unit from a
+// global counter whenever it starts loading one, so the SMs finish together.
+// TMEM is allocated and the barriers set up once, the next unit's Q / dO
+// tiles load while the current unit runs, and the K / V ring, the S / dP
+// buffers and their barrier phases simply continue across units (counted by
+// one step counter m).  The producer publishes each claimed unit (or -1 when
+// none is left) in shared memory with the Q / dO load, and loads the next
+// unit's Q / dO only once every other warp has taken the current one
+// (unit_free): so no per-unit barrier can run two phases ahead of a warp that
+// waits on it, units without active tiles included.  Between units the
+// epilogue of unit j and the first dQ MMA of unit j + 1 meet at acc_empty.
 //
 // TMEM columns (512): dQ accumulator [0,128), Q [128,192), dO [192,256)
 // (16-bit pairs), and two S/dP buffers of 128 columns at 256 and 384 (S in
@@ -28,12 +41,10 @@
 // the 16 keys of MMA K-step kk sit at buffer column 32 (kk / 2) + 8 (kk % 2).
 //
 // Three warps issue MMAs into the one tensor pipe: warp 1 S(m), warp 2 dP(m),
-// warp 3 the accumulation dQ(n).  The pipe accepts only a few MMAs ahead of
-// the one executing and a barrier wait costs a few hundred cycles while the
-// softmax warps keep the SM busy, so with a single issuer every wait drained
-// the pipe; with several, one warp's MMAs keep it fed while another waits.
-// S(m) waits for dQ(m-2), which read dS(m-2) from the same buffer; dP(m)
-// waits for the softmax warps to have read dP(m-2); dQ(n) waits for dS(n).
+// warp 3 the accumulation dQ(n), each waiting only on its own inputs.  The
+// pipe accepts only a few MMAs ahead of the one executing and a barrier wait
+// costs a few hundred cycles while the softmax warps keep the SM busy, so
+// with a single issuer every wait drained the pipe.
 //
 // Warp roles (384 threads): warp 0 issues TMA loads, warp 1 owns TMEM and
 // issues S, warp 2 issues dP, warp 3 issues dQ (whole warps, one elected
@@ -50,48 +61,71 @@ namespace mab {
 
 namespace dq_side {
 
-constexpr int STAGES = 6;     // K/V ring depth; stages 4 and 5 reuse the Q / dO tiles
+constexpr int STAGES = 5;     // K/V ring depth
 constexpr int COL_ACC = 0;    // dQ accumulator, 128 fp32 columns
 constexpr int COL_QA = 128;   // Q as the A operand, 64 columns of 16-bit pairs
 constexpr int COL_DOA = 192;  // dO as the A operand
 constexpr int COL_BUF = 256;  // buffer b: S at COL_BUF + 128 b, dP at +64
+constexpr int SM_WARP0 = 4;   // first softmax warp
 constexpr int SM_WARPS = 8;   // softmax warps
-constexpr int SM_WARP0 = 4;     // first softmax warp
 constexpr int NUM_THREADS = 32 * (SM_WARP0 + SM_WARPS);
 
 struct __align__(1024) Smem {
-  uint8_t Q[2 * Q_TILE * 128];  // two 64-column chunks, 128B swizzle; later K/V stage 4
-  uint8_t dO[2 * Q_TILE * 128]; // later K/V stage 5
-  uint8_t K[STAGES - 2][2 * Q_SUB * 128];
-  uint8_t V[STAGES - 2][2 * Q_SUB * 128];
+  uint8_t Q[2 * Q_TILE * 128];  // two 64-column chunks, 128B swizzle; once copied
+                                // into TMEM, the epilogue staging (4 KB per warp)
+  uint8_t dO[2 * Q_TILE * 128];
+  uint8_t K[STAGES][2 * Q_SUB * 128];
+  uint8_t V[STAGES][2 * Q_SUB * 128];
   int step_t[STAGES];           // key sub-tile of the step in the stage
-  uint64_t bar_q_full;          // Q, dO landed in shared memory
+  int unit;                     // unit of the latest Q / dO load, -1: none left
+  uint64_t bar_q_full;          // Q, dO of the unit landed in shared memory
   uint64_t bar_qa_full;         // Q, dO copied into TMEM (all softmax warps)
   uint64_t bar_kv_full[STAGES];
   uint64_t bar_kv_empty[STAGES];
   uint64_t bar_s_full[2];       // S and dP of the buffer complete (one commit each)
   uint64_t bar_p_full[2];       // dS of the buffer packed (all softmax warps)
   uint64_t bar_acc_free[2];     // dQ MMA that read the buffer's dS complete
-  uint64_t bar_x_done[2];       // every S (0) / dP (1) MMA complete
-  uint64_t bar_acc_full;
+  uint64_t bar_acc_full;        // every dQ MMA of the unit complete
+  uint64_t bar_acc_empty;       // the unit's accumulator read and stored (all softmax warps)
+  uint64_t bar_unit_free;       // every other warp took the unit (and, softmax warps,
+                                // stored the previous unit's epilogue)
+  uint64_t bar_x_done[3];       // every MMA of the S / dP / dQ warp complete
   uint32_t tmem_base;
   int abort_flag;
 };
 
 constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
-static_assert(2 * Q_TILE * 128 == 2 * (2 * Q_SUB * 128), "a K/V stage must fit in a Q tile");
-
-// K / V tile of stage st (stages 4 and 5 live in the Q and dO tiles once
-// those are in TMEM).
-__device__ __forceinline__ uint8_t* stage_k(Smem& s, int st) {
-  return st < STAGES - 2 ? s.K[st] : (st == STAGES - 2 ? s.Q : s.dO);
-}
-__device__ __forceinline__ uint8_t* stage_v(Smem& s, int st) {
-  return st < STAGES - 2 ? s.V[st] : (st == STAGES - 2 ? s.Q : s.dO) + 2 * Q_SUB * 128;
-}
 
 enum { TAG_Q = 0x301, TAG_QA, TAG_KV_EMPTY, TAG_KV_FULL, TAG_P_FULL, TAG_S_FULL, TAG_ACC_FREE,
-       TAG_ACC, TAG_X_DONE };
+       TAG_ACC, TAG_X_DONE, TAG_ACC_EMPTY, TAG_UNIT_FREE };
+
+// Stage of the K/V ring and the parity of its current use (kept as counters:
+// STAGES is not a power of two).
+struct Ring {
+  int st = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next() {
+    if (++st == STAGES) {
+      st = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
+// Coordinates of work unit u: heaviest causal query tiles first.
+struct DqUnit {
+  int bh, q0, kvh, h;
+  QWalk walk;
+  __device__ __forceinline__ void init(const AttnParams& p, int u) {
+    const int BH = p.B * p.Hq;
+    const int qt = p.nQT_q - 1 - u / BH;
+    bh = u % BH;
+    h = bh % p.Hq;
+    kvh = (bh / p.Hq) * p.Hkv + h / p.group;
+    q0 = qt * Q_TILE;
+    walk.init(p, bh, qt);
+  }
+};
 
 }  // namespace dq_side
 
@@ -105,15 +139,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int BH = p.B * p.Hq;
-  const int qt = p.nQT_q - 1 - (int)(blockIdx.x / BH);  // longest causal rows first
-  const int bh = (int)(blockIdx.x % BH);
-  const int b = bh / p.Hq, h = bh % p.Hq;
-  const int kvh = b * p.Hkv + h / p.group;
-  const int q0 = qt * Q_TILE;
-  QWalk walk;
-  walk.init(p, bh, qt);
-  const int N = walk.cnt;
+  const int U = p.nQT_q * p.B * p.Hq;
   WaitCtx wc{p.status, &s.abort_flag, p.timeout_ns};
 
   if (threadIdx.x == 0) {
@@ -129,9 +155,10 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       mbar_init(smem_u32(&s.bar_p_full[i]), SM_WARPS);
       mbar_init(smem_u32(&s.bar_acc_free[i]), 1);
     }
-    mbar_init(smem_u32(&s.bar_x_done[0]), 1);
-    mbar_init(smem_u32(&s.bar_x_done[1]), 1);
     mbar_init(smem_u32(&s.bar_acc_full), 1);
+    mbar_init(smem_u32(&s.bar_acc_empty), SM_WARPS);
+    mbar_init(smem_u32(&s.bar_unit_free), SM_WARPS + 3);
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&s.bar_x_done[i]), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -150,199 +177,268 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       tma_prefetch_desc(&tdO);
       tma_prefetch_desc(&tK);
       tma_prefetch_desc(&tV);
+      bool ok = true;
+      int m = 0;  // step counter across units
+      Ring rg;
       const uint32_t qbar = smem_u32(&s.bar_q_full);
-      mbar_arrive_expect_tx(qbar, 4 * Q_TILE * 128);
-      tma_load_3d(smem_u32(s.Q), &tQ, 0, q0, bh, qbar);
-      tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, q0, bh, qbar);
-      tma_load_3d(smem_u32(s.dO), &tdO, 0, q0, bh, qbar);
-      tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, q0, bh, qbar);
-      for (int n = 0; n < N; ++n) {
-        const int st = n % STAGES;
-        if (n >= STAGES &&
-            !mbar_wait(smem_u32(&s.bar_kv_empty[st]), ((n / STAGES) - 1) & 1, wc, TAG_KV_EMPTY))
+      for (int j = 0; ok; ++j) {
+        // the Q / dO tiles and the unit slot are free once every other warp
+        // has taken the previous unit (the softmax warps: copied its Q / dO
+        // into TMEM and stored the epilogue before it, staged in the Q tile)
+        if (j >= 1 && !mbar_wait(smem_u32(&s.bar_unit_free), (j - 1) & 1, wc, TAG_UNIT_FREE))
           break;
-        // stages 4 and 5 overwrite the Q / dO tiles: wait until every softmax
-        // warp has copied them into TMEM
-        if (n == STAGES - 2 && !mbar_wait(smem_u32(&s.bar_qa_full), 0, wc, TAG_QA)) break;
-        const int t = walk.tile(n);
-        s.step_t[st] = t;  // published by the arrive below together with the loads
-        const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
-        uint8_t* sk = stage_k(s, st);
-        uint8_t* sv = stage_v(s, st);
-        mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
-        tma_load_3d(smem_u32(sk), &tK, 0, t * Q_SUB, kvh, fb);
-        tma_load_3d(smem_u32(sk + Q_SUB * 128), &tK, 64, t * Q_SUB, kvh, fb);
-        tma_load_3d(smem_u32(sv), &tV, 0, t * Q_SUB, kvh, fb);
-        tma_load_3d(smem_u32(sv + Q_SUB * 128), &tV, 64, t * Q_SUB, kvh, fb);
+        int u = j == 0 ? (int)blockIdx.x : (int)(gridDim.x + atomicAdd(&p.status->next_unit, 1u));
+        if (u >= U) u = -1;
+        s.unit = u;  // published by the arrive on q_full
+        if (u < 0) {
+          mbar_arrive(qbar);
+          break;
+        }
+        DqUnit un;
+        un.init(p, u);
+        mbar_arrive_expect_tx(qbar, 4 * Q_TILE * 128);
+        tma_load_3d(smem_u32(s.Q), &tQ, 0, un.q0, un.bh, qbar);
+        tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, un.q0, un.bh, qbar);
+        tma_load_3d(smem_u32(s.dO), &tdO, 0, un.q0, un.bh, qbar);
+        tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, un.q0, un.bh, qbar);
+        for (int n = 0; n < un.walk.cnt; ++n, ++m, rg.next()) {
+          const int st = rg.st;
+          if (m >= STAGES &&
+              !mbar_wait(smem_u32(&s.bar_kv_empty[st]), rg.ph ^ 1u, wc,
+                         TAG_KV_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const int t = un.walk.tile(n);
+          s.step_t[st] = t;  // published by the arrive below together with the loads
+          const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
+          mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
+          tma_load_3d(smem_u32(s.K[st]), &tK, 0, t * Q_SUB, un.kvh, fb);
+          tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, t * Q_SUB, un.kvh, fb);
+          tma_load_3d(smem_u32(s.V[st]), &tV, 0, t * Q_SUB, un.kvh, fb);
+          tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, t * Q_SUB, un.kvh, fb);
+        }
       }
     }
   } else if (warp >= 1 && warp < SM_WARP0) {
     // ------------------------------------------------------------ MMA issuers (whole warps)
     constexpr uint32_t ID_S = idesc_f16(BF16, Q_TILE, Q_SUB, false, false);
     constexpr uint32_t ID_ACC = idesc_f16(BF16, Q_TILE, HEAD_DIM, false, true);
+    bool ok = true;
+    int m = 0;  // step counter across units
+    Ring rg;
     if (warp == 1 || warp == 2) {
       // warp 1: S(m) = Q K^T into the S half of buffer m & 1; warp 2: dP(m) =
       // dO V^T into its dP half (A = Q / dO from TMEM, B = K / V tile, K-major)
       const bool is_s = warp == 1;
       const uint32_t a0 = tbase + (is_s ? COL_QA : COL_DOA);
-      bool ok = N == 0 || mbar_wait_warp(smem_u32(&s.bar_qa_full), 0, wc, TAG_QA);
-      for (int m = 0; ok && m < N; ++m) {
-        const int bf = m & 1, st = m % STAGES;
-        ok = mbar_wait_warp(smem_u32(&s.bar_kv_full[st]), (m / STAGES) & 1, wc, TAG_KV_FULL);
-        if (ok && m >= 2) {
-          // S half: held dS(m - 2), read by dQ(m - 2); dP half: read by the
-          // softmax warps before they signalled step m - 2
-          ok = is_s ? mbar_wait_warp(smem_u32(&s.bar_acc_free[bf]), ((m - 2) >> 1) & 1, wc,
-                                     TAG_ACC_FREE)
-                    : mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), ((m - 2) >> 1) & 1, wc,
-                                     TAG_P_FULL);
+      for (int j = 0; ok; ++j) {
+        if (!mbar_wait_warp(smem_u32(&s.bar_q_full), j & 1, wc, TAG_Q)) break;
+        const int u = s.unit;
+        if (u < 0) break;
+        DqUnit un;
+        un.init(p, u);
+        const int N = un.walk.cnt;
+        ok = mbar_wait_warp(smem_u32(&s.bar_qa_full), j & 1, wc, TAG_QA);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.bar_unit_free));
+        for (int n = 0; ok && n < N; ++n, ++m, rg.next()) {
+          const int bf = m & 1, st = rg.st;
+          ok = mbar_wait_warp(smem_u32(&s.bar_kv_full[st]), rg.ph, wc, TAG_KV_FULL);
+          if (ok && m >= 2) {
+            // S half: held dS(m - 2), read by dQ(m - 2); dP half: read by the
+            // softmax warps before they signalled step m - 2
+            ok = is_s ? mbar_wait_warp(smem_u32(&s.bar_acc_free[bf]), ((m - 2) >> 1) & 1, wc,
+                                       TAG_ACC_FREE)
+                      : mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), ((m - 2) >> 1) & 1, wc,
+                                       TAG_P_FULL);
+          }
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d = tbase + COL_BUF + bf * 128 + (is_s ? 0 : 64);
+          const uint64_t bB = sdesc_sw128(smem_u32(is_s ? s.K[st] : s.V[st]), 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+            mma_ts_w(d, a0 + 8 * kk,
+                     bB + (uint64_t)(((kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                     kk > 0 ? 1u : 0u);
+          mma_commit_w(smem_u32(&s.bar_s_full[bf]));
         }
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d = tbase + COL_BUF + bf * 128 + (is_s ? 0 : 64);
-        const uint64_t bB = sdesc_sw128(smem_u32(is_s ? stage_k(s, st) : stage_v(s, st)), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-          mma_ts_w(d, a0 + 8 * kk,
-                   bB + (uint64_t)(((kk >> 2) * (Q_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                   kk > 0 ? 1u : 0u);
-        mma_commit_w(smem_u32(&s.bar_s_full[bf]));
       }
-      // this warp's MMAs must be complete before TMEM is freed (abort path)
-      mma_commit_w(smem_u32(&s.bar_x_done[is_s ? 0 : 1]));
-      mbar_wait_warp(smem_u32(&s.bar_x_done[is_s ? 0 : 1]), 0, wc, TAG_X_DONE);
     } else {
-      // dQ += dS(n) K (A = dS packed in buffer n & 1, B = K tile, MN-major)
-      bool ok = true;
-      for (int n = 0; ok && n < N; ++n) {
-        const int bf = n & 1, st = n % STAGES;
-        ok = mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), (n >> 1) & 1, wc, TAG_P_FULL);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t a = tbase + COL_BUF + bf * 128;
-        const uint64_t bK = sdesc_sw128(smem_u32(stage_k(s, st)), Q_SUB * 128, 1024);
+      // dQ += dS(n) K (A = dS packed in buffer m & 1, B = K tile, MN-major)
+      for (int j = 0; ok; ++j) {
+        // the unit's first accumulation overwrites the accumulator: the
+        // softmax warps must have read the previous unit's
+        if (j >= 1 &&
+            !mbar_wait_warp(smem_u32(&s.bar_acc_empty), (j - 1) & 1, wc, TAG_ACC_EMPTY))
+          break;
+        if (!mbar_wait_warp(smem_u32(&s.bar_q_full), j & 1, wc, TAG_Q)) break;
+        const int u = s.unit;
+        if (u < 0) break;
+        DqUnit un;
+        un.init(p, u);
+        const int N = un.walk.cnt;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.bar_unit_free));
+        for (int n = 0; ok && n < N; ++n, ++m, rg.next()) {
+          const int bf = m & 1, st = rg.st;
+          ok = mbar_wait_warp(smem_u32(&s.bar_p_full[bf]), (m >> 1) & 1, wc, TAG_P_FULL);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a = tbase + COL_BUF + bf * 128;
+          const uint64_t bK = sdesc_sw128(smem_u32(s.K[st]), Q_SUB * 128, 1024);
 #pragma unroll
-        for (int kk = 0; kk < Q_SUB / 16; ++kk)
-          mma_ts_w(tbase + COL_ACC, a + 32 * (kk >> 1) + 8 * (kk & 1), bK + (uint64_t)((kk * 2048) >> 4), ID_ACC,
-                   (n > 0 || kk > 0) ? 1u : 0u);
-        // S(n) and dP(n) completed before the softmax warps could signal step
-        // n, so this commit also frees the K / V stage
-        mma_commit_w(smem_u32(&s.bar_kv_empty[st]));
-        mma_commit_w(smem_u32(&s.bar_acc_free[bf]));
+          for (int kk = 0; kk < Q_SUB / 16; ++kk)
+            mma_ts_w(tbase + COL_ACC, a + 32 * (kk >> 1) + 8 * (kk & 1),
+                     bK + (uint64_t)((kk * 2048) >> 4), ID_ACC, (n > 0 || kk > 0) ? 1u : 0u);
+          // S(m) and dP(m) completed before the softmax warps could signal
+          // step m, so this commit also frees the K / V stage
+          mma_commit_w(smem_u32(&s.bar_kv_empty[st]));
+          mma_commit_w(smem_u32(&s.bar_acc_free[bf]));
+        }
+        if (ok) mma_commit_w(smem_u32(&s.bar_acc_full));  // the unit's accumulator is complete
       }
-      // completes when every MMA issued above has (also on the abort path, so
-      // that TMEM is idle before it is freed)
-      mma_commit_w(smem_u32(&s.bar_acc_full));
-      mbar_wait_warp(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
     }
+    // this warp's MMAs must be complete before TMEM is freed (also on the
+    // abort path)
+    const uint32_t done = smem_u32(&s.bar_x_done[warp - 1]);
+    mma_commit_w(done);
+    mbar_wait_warp(done, 0, wc, TAG_X_DONE);
   } else {
     // ------------------------------------------------------------ softmax warps
     const int sp = warp & 3, g = (warp - SM_WARP0) >> 2;
     const int rloc = sp * 32 + lane;
-    const int i = q0 + rloc;
     const uint32_t lane_base = tbase + ((uint32_t)(sp * 32) << 16);
-    bool ok = mbar_wait(smem_u32(&s.bar_q_full), 0, wc, TAG_Q);
-    if (ok) {
-      // Q and dO rows into TMEM as 16-bit pairs (element 2c in the low half
-      // of column c): this warp copies d columns 64 g .. 64 g + 63 of its rows.
-      const uint8_t* src[2] = {s.Q + g * (Q_TILE * 128) + rloc * 128,
-                               s.dO + g * (Q_TILE * 128) + rloc * 128};
-      const uint32_t dst[2] = {COL_QA + 32u * g, COL_DOA + 32u * g};
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        uint32_t w[32];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src[which] + ((u ^ (rloc & 7)) << 4));
-          w[4 * u] = v.x;
-          w[4 * u + 1] = v.y;
-          w[4 * u + 2] = v.z;
-          w[4 * u + 3] = v.w;
-        }
-        tmem_st32(lane_base + dst[which], w);
-      }
-      tmem_wait_st();
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&s.bar_qa_full));
-
-    const size_t srow = (size_t)bh * p.Sq_pad + i;
-    const float lse2_i = p.lse2[srow];
-    const float delta_i = p.delta[srow];
-    int flo, fhi;  // key sub-tiles that are entirely visible
-    full_range_q(p.mask_kind, p.window, p.Sq, p.Skv, q0, &flo, &fhi);
-    for (int n = 0; ok && n < N; ++n) {
-      const int bf = n & 1, st = n % STAGES;
-      // s_full implies the stage's loads landed; waiting on kv_full as well
-      // makes the step's tile index (written by the producer) visible
-      if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (n >> 1) & 1, wc, TAG_S_FULL) ||
-          !mbar_wait(smem_u32(&s.bar_kv_full[st]), (n / STAGES) & 1, wc, TAG_KV_FULL)) {
-        ok = false;
-        break;
-      }
+    uint8_t* stage = s.Q + (warp - SM_WARP0) * 4096;
+    // Reads (or zero-fills) the accumulator of unit j, writes the unit's dQ
+    // columns [64 g, 64 g + 64) of this warp's 32 rows and releases both the
+    // accumulator and the staging space.
+    auto epilogue = [&](int j, const DqUnit& un, bool ok) {
+      uint32_t pk[32];
+      bool have = ok && mbar_wait(smem_u32(&s.bar_acc_full), j & 1, wc, TAG_ACC);
+      have = have && un.walk.cnt > 0;
       tc_fence_after();
-      const uint32_t col = COL_BUF + bf * 128 + 32 * g;
-      float sv[32], dp[32];
-      tmem_ld32(lane_base + col, sv);
-      tmem_ld32(lane_base + col + 64, dp);
-      const int t = s.step_t[st];
-      // warp-uniform: the whole 128 x 64 sub-tile is visible
-      const bool full = t >= flo && t <= fhi;
-      const uint32_t vis = full ? 0xffffffffu : vis_query_row(p, bh, i, t * Q_SUB + 32 * g);
-      tmem_wait_ld_regs(sv);
+      if (have) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c) asm volatile("" : "+f"(dp[c]));
-      uint32_t pk[16];
-      if (full) {
+        for (int half = 0; half < 2; ++half) {
+          float v[32];
+          tmem_ld32(lane_base + COL_ACC + 64 * g + 32 * half, v);
+          tmem_wait_ld_regs(v);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -lse2_i));
-          const float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -lse2_i));
-          pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
+          for (int c = 0; c < 16; ++c)
+            pk[16 * half + c] = pack2<BF16>(v[2 * c] * p.scale, v[2 * c + 1] * p.scale);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -lse2_i));
-          float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -lse2_i));
-          p0 = ((vis >> (2 * c)) & 1u) ? p0 : 0.f;
-          p1 = ((vis >> (2 * c + 1)) & 1u) ? p1 : 0.f;
-          pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
-        }
+        for (int c = 0; c < 32; ++c) pk[c] = 0u;
       }
-      tmem_st16(lane_base + col, pk);
-      tmem_wait_st();
+      const int r0 = un.q0 + sp * 32;
+      uint16_t* orow = dq + ((size_t)un.bh * p.Sq + r0) * HEAD_DIM + 64 * g;
+      warp_store_rows(stage, pk, orow, min(32, p.Sq - r0));
+      // the next TMA load into the Q tile comes after this warp's generic
+      // accesses to it
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&s.bar_p_full[bf]));
-    }
-    // ---------------------------------------------------------- epilogue
-    // Columns [64 g, 64 g + 64) of the accumulator, one row per lane.
-    uint32_t pk[32];
-    bool have = ok && N > 0;
-    if (have) have = mbar_wait(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
-    tc_fence_after();
-    if (have) {
+      if (lane == 0) mbar_arrive(smem_u32(&s.bar_acc_empty));
+    };
+    bool ok = true;
+    int m = 0;  // step counter across units
+    Ring rg;
+    DqUnit prev;
+    int j = 0;
+    for (; ok; ++j) {
+      ok = mbar_wait(smem_u32(&s.bar_q_full), j & 1, wc, TAG_Q);
+      const int u = ok ? s.unit : -1;
+      if (u < 0) break;
+      DqUnit un;
+      un.init(p, u);
+      // Q and dO rows of the unit into TMEM as 16-bit pairs (element 2c in
+      // the low half of column c): this warp copies d columns
+      // 64 g .. 64 g + 63 of its rows.  Every S / dP MMA of the previous unit
+      // completed before its last step was signalled, so the columns are free.
+      {
+        const uint8_t* src[2] = {s.Q + g * (Q_TILE * 128) + rloc * 128,
+                                 s.dO + g * (Q_TILE * 128) + rloc * 128};
+        const uint32_t dst[2] = {COL_QA + 32u * g, COL_DOA + 32u * g};
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float v[32];
-        tmem_ld32(lane_base + COL_ACC + 64 * g + 32 * half, v);
-        tmem_wait_ld_regs(v);
+        for (int which = 0; which < 2; ++which) {
+          uint32_t w[32];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[16 * half + c] = pack2<BF16>(v[2 * c] * p.scale, v[2 * c + 1] * p.scale);
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src[which] + ((c ^ (rloc & 7)) << 4));
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+          }
+          tmem_st32(lane_base + dst[which], w);
+        }
+        tmem_wait_st();
       }
-    } else {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s.bar_qa_full));
+      // the previous unit's epilogue overlaps this unit's first MMAs
+      if (j >= 1) epilogue(j - 1, prev, ok);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&s.bar_unit_free));
+
+      const int i = un.q0 + rloc;
+      const size_t srow = (size_t)un.bh * p.Sq_pad + i;
+      const float lse2_i = p.lse2[srow];
+      const float delta_i = p.delta[srow];
+      int flo, fhi;  // key sub-tiles that are entirely visible
+      full_range_q(p.mask_kind, p.window, p.Sq, p.Skv, un.q0, &flo, &fhi);
+      for (int n = 0; ok && n < un.walk.cnt; ++n, ++m, rg.next()) {
+        const int bf = m & 1, st = rg.st;
+        // s_full implies the stage's loads landed; waiting on kv_full as well
+        // makes the step's tile index (written by the producer) visible
+        if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (m >> 1) & 1, wc, TAG_S_FULL) ||
+            !mbar_wait(smem_u32(&s.bar_kv_full[st]), rg.ph, wc, TAG_KV_FULL)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t col = COL_BUF + bf * 128 + 32 * g;
+        float sv[32], dp[32];
+        tmem_ld32(lane_base + col, sv);
+        tmem_ld32(lane_base + col + 64, dp);
+        const int t = s.step_t[st];
+        // warp-uniform: the whole 128 x 64 sub-tile is visible
+        const bool full = t >= flo && t <= fhi;
+        const uint32_t vis = full ? 0xffffffffu : vis_query_row(p, un.bh, i, t * Q_SUB + 32 * g);
+        tmem_wait_ld_regs(sv);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = 0u;
+        for (int c = 0; c < 32; ++c) asm volatile("" : "+f"(dp[c]));
+        uint32_t pk[16];
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -lse2_i));
+            const float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -lse2_i));
+            pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -lse2_i));
+            float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -lse2_i));
+            p0 = ((vis >> (2 * c)) & 1u) ? p0 : 0.f;
+            p1 = ((vis >> (2 * c + 1)) & 1u) ? p1 : 0.f;
+            pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
+          }
+        }
+        tmem_st16(lane_base + col, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&s.bar_p_full[bf]));
+      }
+      prev = un;
     }
-    // Every MMA has completed (or none was issued), so no stage is being
-    // read or loaded: the first two K tiles stage the output rows.
-    named_bar_sync(1, 32 * SM_WARPS);
-    uint8_t* stage = s.K[0] + (warp - SM_WARP0) * 4096;
-    const int r0 = q0 + sp * 32;
-    uint16_t* orow = dq + ((size_t)bh * p.Sq + r0) * HEAD_DIM + 64 * g;
-    warp_store_rows(stage, pk, orow, min(32, p.Sq - r0));
+    if (j >= 1) epilogue(j - 1, prev, ok);
   }
   tc_fence_before();
   __syncthreads();
@@ -358,7 +454,12 @@ cudaError_t launch_dq(bool bf16, const AttnParams& p, const CUtensorMap& tQ, con
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dq_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(p.nQT_q * p.B * p.Hq));
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int units = p.nQT_q * p.B * p.Hq;
+  dim3 grid((unsigned)(units < sms ? units : sms));
   kern<<<grid, dq_side::NUM_THREADS, dq_side::SMEM_BYTES, st>>>(tQ, tdO, tK, tV, (uint16_t*)dq,
                                                                  p);
   return cudaGetLastError();

@@ -19,7 +19,7 @@ struct DevStatus {
   unsigned int code;      // 0 = ok, else an attn_status_t value
   unsigned int where;     // which wait gave up (kernel-specific tag)
   unsigned int block;     // blockIdx.x of the first CTA that gave up
-  unsigned int pad;
+  unsigned int next_unit;  // work counter of the persistent kernels (zeroed with the rest)
 };
 
 struct WaitCtx {
