@@ -95,6 +95,7 @@ struct __align__(1024) Smem {
 };
 
 constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
+static_assert(SMEM_BYTES <= 232448, "over the 227 KB of shared memory a CTA may use");
 
 enum { TAG_Q = 0x301, TAG_QA, TAG_KV_EMPTY, TAG_KV_FULL, TAG_P_FULL, TAG_S_FULL, TAG_ACC_FREE,
        TAG_ACC, TAG_X_DONE, TAG_ACC_EMPTY, TAG_UNIT_FREE };

@@ -92,6 +92,7 @@ struct __align__(1024) Smem {
 };
 
 constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
+static_assert(SMEM_BYTES <= 232448, "over the 227 KB of shared memory a CTA may use");
 static_assert(2 * KV_TILE * 128 == 2 * (2 * KV_SUB * 128), "stage 4 must fit in K's tile");
 
 // Q / dO tile of stage st (stage STAGES - 1 lives in K's tile once K is in TMEM).
