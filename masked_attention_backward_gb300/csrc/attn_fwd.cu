@@ -458,18 +458,18 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
         float mp[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c) mp[c] = -INFINITY;
-        if (full) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) mp[c & 7] = fmaxf(mp[c & 7], sv[c]);
-        } else {
+        if (!full) {
+          // invisible logits drop out of the maximum
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            mp[c & 7] = ((vis0 >> c) & 1u) ? fmaxf(mp[c & 7], sv[c]) : mp[c & 7];
-            mp[(c + 4) & 7] = ((vis1 >> c) & 1u) ? fmaxf(mp[(c + 4) & 7], sv[32 + c]) : mp[(c + 4) & 7];
+            sv[c] = ((vis0 >> c) & 1u) ? sv[c] : -INFINITY;
+            sv[32 + c] = ((vis1 >> c) & 1u) ? sv[32 + c] : -INFINITY;
           }
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+#pragma unroll
+        for (int c = 0; c < 32; ++c) mp[c & 7] = fmax3f(mp[c & 7], sv[2 * c], sv[2 * c + 1]);
+        const float mx = fmax3f(fmax3f(mp[0], mp[1], mp[2]), fmax3f(mp[3], mp[4], mp[5]),
+                                fmaxf(mp[6], mp[7]));
         const float mx2 = mx == -INFINITY ? -INFINITY : mx * p.scale_log2;
         // move M when the row maximum exceeds it by more than 8; a row that
         // has seen nothing yet (M = -inf, so O and l are still zero) just
@@ -480,32 +480,24 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
           M = mx2;
           l *= alpha;
         }
+        // P = exp2(S scale log2e - M): an invisible logit (-inf here) gives 0;
+        // a row with nothing visible keeps M = -inf and all its logits at
+        // -inf, and the finite stand-in keeps -inf - (-inf) out
+        const float Ms = M == -INFINITY ? 0.f : M;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-Ms, -Ms);
         uint32_t pk[32];
-        float lp[8];
+        float2 lp[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) lp[c] = 0.f;
-        if (full) {
+        for (int c = 0; c < 4; ++c) lp[c] = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -M));
-            const float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -M));
-            lp[c & 7] += p0 + p1;
-            pk[c] = pack2<BF16>(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const uint32_t vis = c < 16 ? vis0 : vis1;
-            const int b0 = (2 * c) & 31;
-            float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -M));
-            float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -M));
-            p0 = ((vis >> b0) & 1u) ? p0 : 0.f;
-            p1 = ((vis >> (b0 + 1)) & 1u) ? p1 : 0.f;
-            lp[c & 7] += p0 + p1;
-            pk[c] = pack2<BF16>(p0, p1);
-          }
+        for (int c = 0; c < 32; ++c) {
+          const float2 x = ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sc2, nm2);
+          const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          lp[c & 3] = fadd2(lp[c & 3], pp);
+          pk[c] = pack2<BF16>(pp.x, pp.y);
         }
-        l += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
+        const float2 ls = fadd2(fadd2(lp[0], lp[1]), fadd2(lp[2], lp[3]));
+        l += ls.x + ls.y;
         // rescale this group's O rows whose M moved, once the group's
         // previous O += P V of the unit has completed (the unit's first
         // accumulation of the group overwrites instead)
