@@ -85,7 +85,7 @@ WsLayout layout_of(const attn_shape_t* sh, const attn_mask_desc_t* mk) {
   size_t off = 0;
   L.status = off;
   off = align256(off + sizeof(DevStatus));
-  L.lse2 = off;
+  L.nlse2 = off;
   off = align256(off + BH * d.Sq_pad * sizeof(float));
   L.delta = off;
   off = align256(off + BH * d.Sq_pad * sizeof(float));
@@ -147,7 +147,7 @@ AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const W
   p.nKT_k = d.nKT_k;
   p.nQT_q = d.nQT_q;
   p.nKT_q = d.nKT_q;
-  p.lse2 = reinterpret_cast<const float*>(ws + L.lse2);
+  p.nlse2 = reinterpret_cast<const float*>(ws + L.nlse2);
   p.delta = reinterpret_cast<const float*>(ws + L.delta);
   p.scale = scale;
   p.scale_log2 = scale * LOG2E;
@@ -307,7 +307,7 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
   cudaError_t e = cudaMemsetAsync(w + L.status, 0, sizeof(DevStatus), st);
   if (e == cudaSuccess) {
     ProfScope ps("k_preprocess", st);
-    e = launch_preprocess(bf16, o, dO, lse, sink, reinterpret_cast<float*>(w + L.lse2),
+    e = launch_preprocess(bf16, o, dO, lse, sink, reinterpret_cast<float*>(w + L.nlse2),
                           reinterpret_cast<float*>(w + L.delta),
                           reinterpret_cast<float*>(w + L.dsink_part), shape->B, shape->Hq,
                           shape->Sq, d.Sq_pad, st);

@@ -4,7 +4,7 @@
 // loaded once and copied into TMEM, where they serve as the A operand of
 // every score contraction.  For each active key sub-tile t of Q_SUB rows:
 //   S  = Q K_t^T,  dP = dO V_t^T                 (A from TMEM, fp32 in TMEM)
-//   P  = exp2(S * scale*log2e - lse2),  dS = P (dP - Delta)   (softmax warps)
+//   P  = exp2(S * scale*log2e - lse log2e),  dS = P (dP - Delta)   (softmax warps)
 //   dQ += dS K_t                                  (A = dS from TMEM)
 // then dQ *= scale, rounded to the input dtype and written once.
 //
@@ -388,7 +388,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
 
       const int i = un.q0 + rloc;
       const size_t srow = (size_t)un.bh * p.Sq_pad + i;
-      const float lse2_i = p.lse2[srow];
+      const float nlse2_i = p.nlse2[srow];  // -lse log2(e)
       const float delta_i = p.delta[srow];
       int flo, fhi;  // key sub-tiles that are entirely visible
       full_range_q(p.mask_kind, p.window, p.Sq, p.Skv, un.q0, &flo, &fhi);
@@ -417,15 +417,15 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         if (full) {
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            const float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -lse2_i));
-            const float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -lse2_i));
+            const float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, nlse2_i));
+            const float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, nlse2_i));
             pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
           }
         } else {
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, -lse2_i));
-            float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, -lse2_i));
+            float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, nlse2_i));
+            float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, nlse2_i));
             p0 = ((vis >> (2 * c)) & 1u) ? p0 : 0.f;
             p1 = ((vis >> (2 * c + 1)) & 1u) ? p1 : 0.f;
             pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));

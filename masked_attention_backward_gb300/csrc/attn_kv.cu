@@ -7,7 +7,7 @@
 // for block masks):
 //   S^T  = K Q_r^T            (A = K from TMEM)
 //   dP^T = V dO_r^T           (A = V from shared memory)
-//   P^T  = exp2(S^T * scale*log2e - lse2_r),  dS^T = P^T (dP^T - Delta_r)
+//   P^T  = exp2(S^T * scale*log2e - lse_r log2e),  dS^T = P^T (dP^T - Delta_r)
 //   dV  += P^T dO_r,  dK += dS^T Q_r          (A = P^T / dS^T from TMEM)
 // The group reduction happens in the TMEM accumulators; the epilogue scales
 // dK, rounds both to the input dtype and writes each row once, contiguously.
@@ -69,7 +69,7 @@ struct __align__(1024) Smem {
   uint8_t V[2 * KV_TILE * 128];
   uint8_t Q[STAGES - 1][2 * KV_SUB * 128];
   uint8_t dO[STAGES - 1][2 * KV_SUB * 128];
-  float lse2[STAGES][KV_SUB];
+  float nlse2[STAGES][KV_SUB];  // -lse log2(e) of the stage's query rows
   float delta[STAGES][KV_SUB];
   int step_r[STAGES];            // query sub-tile of the step in the stage
   int step_hh[STAGES];           // its query head within the group
@@ -197,7 +197,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         tma_load_3d(smem_u32(sd), &tdO, 0, r * KV_SUB, bh, fb);
         tma_load_3d(smem_u32(sd + KV_SUB * 128), &tdO, 64, r * KV_SUB, bh, fb);
         const size_t srow = (size_t)bh * p.Sq_pad + (size_t)r * KV_SUB;
-        bulk_load(smem_u32(s.lse2[st]), p.lse2 + srow, KV_SUB * 4, fb);
+        bulk_load(smem_u32(s.nlse2[st]), p.nlse2 + srow, KV_SUB * 4, fb);
         bulk_load(smem_u32(s.delta[st]), p.delta + srow, KV_SUB * 4, fb);
       }
     }
@@ -314,9 +314,9 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     full_range_kv(p.mask_kind, p.window, p.Sq, p.Skv, k0, &flo, &fhi);
     for (int n = 0; ok && n < N; ++n) {
       const int st = n % STAGES;
-      // ---- P^T(n) = exp2(S^T(n) * scale*log2e - lse2)
+      // ---- P^T(n) = exp2(S^T(n) * scale*log2e - lse log2e)
       // s_full implies the stage's loads landed; waiting on q_full as well
-      // makes the bulk-copied lse2 / Delta rows visible to this thread
+      // makes the bulk-copied -lse log2e / Delta rows visible to this thread
       if (!mbar_wait(smem_u32(&s.bar_s_full), n & 1, wc, TAG_S_FULL) ||
           !mbar_wait(smem_u32(&s.bar_q_full[st]), (n / STAGES) & 1, wc, TAG_Q_FULL)) {
         ok = false;
@@ -331,7 +331,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       const uint32_t vis =
           full ? 0xffffu
                : vis_key_row(p, b * p.Hq + c * p.group + s.step_hh[st], j, r * KV_SUB + 16 * g);
-      const float4* l4 = reinterpret_cast<const float4*>(&s.lse2[st][16 * g]);
+      const float4* l4 = reinterpret_cast<const float4*>(&s.nlse2[st][16 * g]);
       float lv[16];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -343,20 +343,22 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       }
       tmem_wait_ld_regs(sv);
       warp_arrive(&s.bar_s_free);  // S^T(n + 1) may overwrite the buffer
+      // an invisible logit becomes -inf, so its P is 0 (and so is its dS)
+      if (!full) {
+#pragma unroll
+        for (int cc = 0; cc < 16; ++cc) sv[cc] = ((vis >> cc) & 1u) ? sv[cc] : -INFINITY;
+      }
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       float pv[16];
       uint32_t pk[8];
-      if (full) {
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) pv[cc] = fast_exp2(fmaf(sv[cc], p.scale_log2, -lv[cc]));
-      } else {
-#pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          const float pe = fast_exp2(fmaf(sv[cc], p.scale_log2, -lv[cc]));
-          pv[cc] = ((vis >> cc) & 1u) ? pe : 0.f;
-        }
+      for (int q = 0; q < 8; ++q) {
+        const float2 x = ffma2(make_float2(sv[2 * q], sv[2 * q + 1]), sc2,
+                               make_float2(lv[2 * q], lv[2 * q + 1]));
+        pv[2 * q] = fast_exp2(x.x);
+        pv[2 * q + 1] = fast_exp2(x.y);
+        pk[q] = pack2<BF16>(pv[2 * q], pv[2 * q + 1]);
       }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) pk[q] = pack2<BF16>(pv[2 * q], pv[2 * q + 1]);
       // dV(n - 1) must have read P^T(n - 1)
       if (n >= 1 && !mbar_wait(smem_u32(&s.bar_pt_free), (n - 1) & 1, wc, TAG_PT_FREE)) {
         ok = false;
@@ -388,9 +390,12 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       tmem_wait_ld_regs(dp);
       warp_arrive(&s.bar_dp_free);  // dP^T(n + 1) may overwrite the buffer
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        pk[q] = pack2<BF16>(pv[2 * q] * (dp[2 * q] - dl[2 * q]),
-                            pv[2 * q + 1] * (dp[2 * q + 1] - dl[2 * q + 1]));
+      for (int q = 0; q < 8; ++q) {
+        const float2 ds = fmul2(make_float2(pv[2 * q], pv[2 * q + 1]),
+                                fsub2(make_float2(dp[2 * q], dp[2 * q + 1]),
+                                      make_float2(dl[2 * q], dl[2 * q + 1])));
+        pk[q] = pack2<BF16>(ds.x, ds.y);
+      }
       // dK(n - 1) must have read dS^T(n - 1)
       if (n >= 1 && !mbar_wait(smem_u32(&s.bar_dst_free), (n - 1) & 1, wc, TAG_DST_FREE)) {
         ok = false;

@@ -25,7 +25,7 @@ enum MaskKind { MK_NONE = 0, MK_CAUSAL = 1, MK_SLIDING = 2, MK_BLOCK = 3 };
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
   size_t status;     // DevStatus
-  size_t lse2;       // float [B*Hq, Sq_pad]: lse * log2(e), padded with +inf
+  size_t nlse2;      // float [B*Hq, Sq_pad]: -lse * log2(e), padded with -inf
   size_t delta;      // float [B*Hq, Sq_pad]: rowsum(dO * O), padded with 0
   size_t dsink_part; // float [Hq, B * n_row_blocks]
   size_t maskT;      // uint8 [B*Hq, nKB, nQB]
@@ -48,7 +48,7 @@ struct AttnParams {
   const int* sel_q;
   const int* cnt_q;
   int nQT_q, nKT_q;
-  const float* lse2;   // [B*Hq, Sq_pad]
+  const float* nlse2;  // [B*Hq, Sq_pad]
   const float* delta;  // [B*Hq, Sq_pad]
   const float* sink;   // forward: [Hq] or nullptr
   float* lse_out;      // forward: [B*Hq, Sq]
@@ -60,7 +60,7 @@ struct AttnParams {
 
 // ---- launchers (each returns the launch error, if any) ----
 cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const float* lse,
-                              const float* sink, float* lse2, float* delta, float* part, int B,
+                              const float* sink, float* nlse2, float* delta, float* part, int B,
                               int Hq, int Sq, int Sq_pad, cudaStream_t st);
 cudaError_t launch_dsink_finalize(const float* part, int Hq, int nparts, float* dsink,
                                   cudaStream_t st);

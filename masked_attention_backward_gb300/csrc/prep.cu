@@ -1,5 +1,5 @@
 // prep.cu -- the memory-bound steps before the two contraction kernels:
-//   k_preprocess      Delta = rowsum(dO * O), lse2 = lse * log2(e) (padded),
+//   k_preprocess      Delta = rowsum(dO * O), nlse2 = -lse * log2(e) (padded),
 //                     and per-block partial sums of exp(sink - lse) * Delta;
 //   k_dsink_finalize  dSink_h = -(fixed-order sum of the partials);
 //   k_mask_transpose  uint8 block mask [BH,nQB,nKB] -> [BH,nKB,nQB];
@@ -25,7 +25,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(256)
 k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
              const float* __restrict__ lse, const float* __restrict__ sink,
-             float* __restrict__ lse2, float* __restrict__ delta, float* __restrict__ part, int Hq,
+             float* __restrict__ nlse2, float* __restrict__ delta, float* __restrict__ part, int Hq,
              int Sq, int Sq_pad, int nparts) {
   constexpr int ROWS_PER_WARP = PREP_ROWS / 8;  // 16
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -69,11 +69,11 @@ k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
       if (row < Sq) {
         float l2 = lse[head_rows + row] * LOG2E;
         delta[o] = acc;
-        lse2[o] = l2;
+        nlse2[o] = -l2;
         if (sink) term_acc += exp2f(sink2 - l2) * acc;
       } else {
         delta[o] = 0.f;
-        lse2[o] = INFINITY;
+        nlse2[o] = -INFINITY;
       }
     }
   }
@@ -180,15 +180,15 @@ __global__ void k_build_sel(AttnParams p, int* __restrict__ sel_k, int* __restri
 }
 
 cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const float* lse,
-                              const float* sink, float* lse2, float* delta, float* part, int B,
+                              const float* sink, float* nlse2, float* delta, float* part, int B,
                               int Hq, int Sq, int Sq_pad, cudaStream_t st) {
   dim3 grid(Sq_pad / PREP_ROWS, B * Hq);
   int nparts = B * (Sq_pad / PREP_ROWS);
   if (bf16)
-    k_preprocess<true><<<grid, 256, 0, st>>>((const uint4*)O, (const uint4*)dO, lse, sink, lse2,
+    k_preprocess<true><<<grid, 256, 0, st>>>((const uint4*)O, (const uint4*)dO, lse, sink, nlse2,
                                               delta, part, Hq, Sq, Sq_pad, nparts);
   else
-    k_preprocess<false><<<grid, 256, 0, st>>>((const uint4*)O, (const uint4*)dO, lse, sink, lse2,
+    k_preprocess<false><<<grid, 256, 0, st>>>((const uint4*)O, (const uint4*)dO, lse, sink, nlse2,
                                                delta, part, Hq, Sq, Sq_pad, nparts);
   return cudaGetLastError();
 }

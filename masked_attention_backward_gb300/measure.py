@@ -40,7 +40,9 @@ def visible_pairs(wl: Workload, block_mask=None) -> int:
 
 def flops(wl: Workload, pairs: int) -> dict:
     D = wl.D
-    return {"total": 10 * D * pairs, "dkdv": 8 * D * pairs, "dq": 6 * D * pairs}
+    # the forward's two contractions (S = Q K^T, O = P V) at 2 D per pair
+    return {"total": 10 * D * pairs, "dkdv": 8 * D * pairs, "dq": 6 * D * pairs,
+            "fwd": 4 * D * pairs}
 
 
 def algorithmic_bytes(wl: Workload, block_mask_bytes: int = 0) -> dict:

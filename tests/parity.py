@@ -120,7 +120,7 @@ def ws_layout(wl: Workload) -> dict:
     BH = wl.B * wl.Hq
     L = {"status": 0}
     off = _a256(16)
-    L["lse2"] = off; off = _a256(off + BH * Sq_pad * 4)
+    L["nlse2"] = off; off = _a256(off + BH * Sq_pad * 4)
     L["delta"] = off; off = _a256(off + BH * Sq_pad * 4)
     L["dsink_part"] = off; off = _a256(off + wl.Hq * wl.B * (Sq_pad // PREP_ROWS) * 4)
     d = {"Sq_pad": Sq_pad, "nQT_k": cdiv(wl.Sq, KV_SUB), "nKT_k": cdiv(wl.Skv, KV_TILE),

@@ -158,7 +158,7 @@ def test_tables_bit_exact(cuda_lib, wl):
     assert np.array_equal(g_cnt_q, cnt_q) and np.array_equal(g_sel_q, sel_q)
 
 
-def test_preprocess_delta_and_lse2(cuda_lib):
+def test_preprocess_delta_and_nlse2(cuda_lib):
     wl = CASES[1]
     inp = make_inputs(wl)
     pb = oracle_problem(wl, inp)
@@ -168,9 +168,9 @@ def test_preprocess_delta_and_lse2(cuda_lib):
     BH, Sp = wl.B * wl.Hq, L["Sq_pad"]
     ws = run.ws.cpu()
     delta = ws_view(ws, L["delta"], BH * Sp, torch.float32).reshape(BH, Sp).double().numpy()
-    lse2 = ws_view(ws, L["lse2"], BH * Sp, torch.float32).reshape(BH, Sp).double().numpy()
+    nlse2 = ws_view(ws, L["nlse2"], BH * Sp, torch.float32).reshape(BH, Sp).double().numpy()
     ref = oracle.delta(pb, O, inp.dO).reshape(BH, wl.Sq)
     assert np.all(np.abs(delta[:, :wl.Sq] - ref) <= 1e-5 * (1 + np.abs(ref)))
-    assert np.all(delta[:, wl.Sq:] == 0) and np.all(np.isposinf(lse2[:, wl.Sq:]))
-    want = lse.double().numpy().reshape(BH, wl.Sq) * np.log2(np.e)
-    assert np.all(np.abs(lse2[:, :wl.Sq] - want) <= 1e-6 * (1 + np.abs(want)))
+    assert np.all(delta[:, wl.Sq:] == 0) and np.all(np.isneginf(nlse2[:, wl.Sq:]))
+    want = -lse.double().numpy().reshape(BH, wl.Sq) * np.log2(np.e)
+    assert np.all(np.abs(nlse2[:, :wl.Sq] - want) <= 1e-6 * (1 + np.abs(want)))
