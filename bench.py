@@ -437,7 +437,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--e2e-chunks", type=int, default=4,
+    ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="runs of GQA groups the host-buffer pipeline overlaps")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -228,19 +228,23 @@ class HostBackward:
 
     The heads of a GQA group are independent of every other group, so the
     call is split into `chunks` runs of whole key/value heads.  Chunk c's
-    inputs are copied in on one stream while chunk c-1 runs attn_bwd on the
-    compute stream and chunk c-2's gradients are copied out on a third; every
-    chunk is one attn_bwd call on pointer offsets into device buffers that are
-    allocated once here (the library itself allocates nothing).  With B > 1 a
-    run of heads is not contiguous across the batch, and dSink sums over the
-    batch, so the call is not split (chunks = 1).
+    inputs are copied in on one stream while earlier chunks run attn_bwd and
+    their gradients are copied out on another; every chunk is one attn_bwd
+    call on pointer offsets into device buffers that are allocated once here
+    (the library itself allocates nothing).  Consecutive chunks alternate
+    between two compute streams, each with a workspace of its own, so that
+    the SMs a chunk leaves idle while its largest key tiles finish take the
+    next chunk's work; small chunks also shorten the first copy, which
+    nothing hides.  With B > 1 a run of heads is not contiguous across the
+    batch, and dSink sums over the batch, so the call is not split
+    (chunks = 1).
 
     __call__ enqueues everything behind the caller's current stream and makes
     that stream wait for the last copy out, so synchronising it covers the
     whole call."""
 
     def __init__(self, B, Hq, Hkv, Sq, Skv, dtype, mask: Mask, scale: float, has_sink: bool,
-                 device, chunks: int = 4):
+                 device, chunks: int = 8):
         self.B, self.Hq, self.Hkv, self.Sq, self.Skv = B, Hq, Hkv, Sq, Skv
         self.dtype, self.mask, self.scale, self.has_sink = dtype, mask, scale, has_sink
         self.device = torch.device(device)
@@ -264,13 +268,15 @@ class HostBackward:
             self.dev["dsink"] = torch.empty(Hq, dtype=torch.float32, device=self.device)
         code = ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16
         self.cshape = attn_shape_t(B, Hq // chunks, kvc, Sq, Skv, D, code)
-        self.ws = workspace(self.cshape, mask, self.device)
+        self.ws = [workspace(self.cshape, mask, self.device) for _ in range(min(2, chunks))]
+        self.s_comp = [torch.cuda.Stream(self.device) for _ in range(min(2, chunks))]
         self.s_in = torch.cuda.Stream(self.device)
         self.s_out = torch.cuda.Stream(self.device)
         self.ev_in = [torch.cuda.Event() for _ in range(chunks)]
         self.ev_done = [torch.cuda.Event() for _ in range(chunks)]
         self.ev_start = torch.cuda.Event()
         self.ev_out = torch.cuda.Event()
+        self.ev_comp = [torch.cuda.Event() for _ in range(len(self.s_comp))]
 
     def bytes_per_call(self, host_in, host_out):
         h2d = sum(t.numel() * t.element_size() for t in host_in.values() if t is not None)
@@ -283,6 +289,8 @@ class HostBackward:
         cur = torch.cuda.current_stream(self.device)
         self.ev_start.record(cur)
         self.s_in.wait_event(self.ev_start)
+        for sc in self.s_comp:
+            sc.wait_event(self.ev_start)
         C, g = self.chunks, self.g
         hq, hk = self.Hq // C, self.Hkv // C
         d = self.dev
@@ -296,7 +304,9 @@ class HostBackward:
                 if self.has_sink:
                     d["sink"][qs].copy_(host_in["sink"][qs], non_blocking=True)
                 self.ev_in[c].record(self.s_in)
-            cur.wait_event(self.ev_in[c])
+            sc = self.s_comp[c % len(self.s_comp)]
+            ws = self.ws[c % len(self.ws)]
+            sc.wait_event(self.ev_in[c])
             mask = self.mask
             if mask.block_mask is not None:
                 mask = Mask(mask.kind, mask.window, mask.bx, mask.by, mask.block_mask[:, qs])
@@ -306,10 +316,10 @@ class HostBackward:
                          _ptr(d["v"][:, ks]), _ptr(d["o"][:, qs]), _ptr(d["dO"][:, qs]),
                          _ptr(d["lse"][:, qs]), _ptr(sink), mask.desc(), self.scale,
                          _ptr(d["dq"][:, qs]), _ptr(d["dk"][:, ks]), _ptr(d["dv"][:, ks]),
-                         _ptr(dsink), _ptr(self.ws), self.ws.numel(), _stream(cur))
+                         _ptr(dsink), _ptr(ws), ws.numel(), _stream(sc))
             if r != ATTN_OK:
                 raise AttnError(r, "attn_bwd")
-            self.ev_done[c].record(cur)
+            self.ev_done[c].record(sc)
             self.s_out.wait_event(self.ev_done[c])
             with torch.cuda.stream(self.s_out):
                 dq, dk, dv, dsink_h = host_out
@@ -320,3 +330,8 @@ class HostBackward:
                     dsink_h[qs].copy_(d["dsink"][qs], non_blocking=True)
         self.ev_out.record(self.s_out)
         cur.wait_event(self.ev_out)
+        # the compute streams are idle once the last copy out has begun; keep
+        # the caller's stream ordered after them too (nothing is pending)
+        for sc, ev in zip(self.s_comp, self.ev_comp):
+            ev.record(sc)
+            cur.wait_event(ev)
