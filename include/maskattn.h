@@ -42,7 +42,12 @@
  * an error nothing is enqueued and the outputs are left untouched.  Device
  * waits inside the kernels are bounded: a wait that runs out records
  * ATTN_ERR_TIMEOUT in the workspace status word, which attn_get_device_status
- * reads back.
+ * reads back.  The limit is 2 s per wait, or MASKATTN_WAIT_TIMEOUT_NS
+ * nanoseconds from the environment at the time of the call.  Test hook:
+ * with MASKATTN_TEST_NO_LOADS=1 in the environment at the time of a call, the
+ * kernels' loader warps issue nothing, so the call's waits run out and it
+ * ends with ATTN_ERR_TIMEOUT (outputs undefined); it exists to exercise this
+ * path and is off unless set.
  */
 #ifndef MASKATTN_H_
 #define MASKATTN_H_

@@ -108,6 +108,15 @@ WsLayout layout_of(const attn_shape_t* sh, const attn_mask_desc_t* mk) {
   return L;
 }
 
+// Test hook (MASKATTN_TEST_NO_LOADS=1): the producer warps of the tcgen05
+// kernels issue no loads and signal nothing, so the first wait of every CTA
+// runs out with nothing in flight -- the way the tests reach the bounded-wait
+// error path without disturbing the GPU.
+int test_no_loads() {
+  const char* e = getenv("MASKATTN_TEST_NO_LOADS");
+  return (e && e[0] == '1') ? 1 : 0;
+}
+
 unsigned long long wait_timeout_ns() {
   const char* e = getenv("MASKATTN_WAIT_TIMEOUT_NS");
   if (e && *e) {
@@ -153,6 +162,7 @@ AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const W
   p.scale_log2 = scale * LOG2E;
   p.status = reinterpret_cast<DevStatus*>(ws + L.status);
   p.timeout_ns = wait_timeout_ns();
+  p.test_no_loads = test_no_loads();
   return p;
 }
 

@@ -179,7 +179,7 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && !p.test_no_loads) {
       tma_prefetch_desc(&tQ);
       tma_prefetch_desc(&tK);
       tma_prefetch_desc(&tV);

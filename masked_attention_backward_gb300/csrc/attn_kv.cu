@@ -160,7 +160,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && !p.test_no_loads) {
       tma_prefetch_desc(&tQ);
       tma_prefetch_desc(&tdO);
       tma_prefetch_desc(&tK);

@@ -56,6 +56,7 @@ struct AttnParams {
   float scale_log2;    // scale * log2(e)
   DevStatus* status;
   unsigned long long timeout_ns;
+  int test_no_loads;   // test hook: the producers issue no loads (every wait runs out)
 };
 
 // ---- launchers (each returns the launch error, if any) ----
