@@ -231,11 +231,11 @@ class HostBackward:
     inputs are copied in on one stream while earlier chunks run attn_bwd and
     their gradients are copied out on another; every chunk is one attn_bwd
     call on pointer offsets into device buffers that are allocated once here
-    (the library itself allocates nothing).  Consecutive chunks alternate
-    between two compute streams, each with a workspace of its own, so that
-    the SMs a chunk leaves idle while its largest key tiles finish take the
-    next chunk's work; small chunks also shorten the first copy, which
-    nothing hides.  With B > 1 a run of heads is not contiguous across the
+    (the library itself allocates nothing).  Consecutive chunks rotate over
+    three compute streams, each with a workspace of its own, so that the SMs
+    a chunk leaves idle while its largest key tiles finish take the next
+    chunks' work; small chunks also shorten the first copy, which nothing
+    hides.  With B > 1 a run of heads is not contiguous across the
     batch, and dSink sums over the batch, so the call is not split
     (chunks = 1).
 
@@ -268,8 +268,8 @@ class HostBackward:
             self.dev["dsink"] = torch.empty(Hq, dtype=torch.float32, device=self.device)
         code = ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16
         self.cshape = attn_shape_t(B, Hq // chunks, kvc, Sq, Skv, D, code)
-        self.ws = [workspace(self.cshape, mask, self.device) for _ in range(min(2, chunks))]
-        self.s_comp = [torch.cuda.Stream(self.device) for _ in range(min(2, chunks))]
+        self.ws = [workspace(self.cshape, mask, self.device) for _ in range(min(3, chunks))]
+        self.s_comp = [torch.cuda.Stream(self.device) for _ in range(min(3, chunks))]
         self.s_in = torch.cuda.Stream(self.device)
         self.s_out = torch.cuda.Stream(self.device)
         self.ev_in = [torch.cuda.Event() for _ in range(chunks)]
