@@ -49,6 +49,7 @@ class _Problem(ctypes.Structure):
         ("bx", ctypes.c_int64), ("by", ctypes.c_int64),
         ("block_mask", ctypes.c_void_p), ("token_mask", ctypes.c_void_p),
         ("sink", ctypes.c_void_p), ("scale", ctypes.c_double),
+        ("seqlen_q", ctypes.c_void_p), ("seqlen_k", ctypes.c_void_p),
     ]
 
 
@@ -135,11 +136,19 @@ class Problem:
     block_mask: Optional[np.ndarray] = None   # uint8 [B,Hq,nQB,nKB]
     token_mask: Optional[np.ndarray] = None   # uint8 [B,Hq,Sq,Skv]
     sink: Optional[np.ndarray] = None         # float64 [Hq] (may hold -inf)
+    seqlen_q: Optional[np.ndarray] = None     # int [B]: valid query rows per batch
+    seqlen_k: Optional[np.ndarray] = None     # int [B]: valid keys per batch
 
     def _c(self):
         self._bm = _u8(self.block_mask)
         self._tm = _u8(self.token_mask)
         self._sk = _f64(self.sink)
+        self._lq = (np.ascontiguousarray(np.asarray(self.seqlen_q, dtype=np.int64))
+                    if self.seqlen_q is not None else None)
+        self._lk = (np.ascontiguousarray(np.asarray(self.seqlen_k, dtype=np.int64))
+                    if self.seqlen_k is not None else None)
+        for a in (self._lq, self._lk):
+            assert a is None or a.size == self.B
         if self.mask_kind == MASK_BLOCK:
             nqb = -(-self.Sq // self.bx)
             nkb = -(-self.Skv // self.by)
@@ -150,7 +159,8 @@ class Problem:
         return ctypes.byref(_Problem(
             self.B, self.Hq, self.Hkv, self.Sq, self.Skv, self.D,
             self.mask_kind, self.window, self.bx, self.by,
-            _ptr(self._bm), _ptr(self._tm), _ptr(self._sk), float(self.scale)))
+            _ptr(self._bm), _ptr(self._tm), _ptr(self._sk), float(self.scale),
+            _ptr(self._lq), _ptr(self._lk)))
 
 
 def forward(pb: Problem, q, k, v, rows=None):

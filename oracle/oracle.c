@@ -27,6 +27,11 @@
  *   LSE_i   = m_i + log(l_i)          (no visible key and no sink: +inf)
  *   O_i     = sum_j exp(s_ij - LSE_i) v_j
  *
+ *   variable lengths (optional per-batch lengths Lq[b] <= Sq, Lk[b] <= Skv):
+ *   rows i >= Lq[b] and keys j >= Lk[b] are outside the problem -- no pair
+ *   with either is visible, such a row has O = 0, LSE = +inf, Delta = 0 and
+ *   no part in dSink, whatever O, dO and LSE the caller passes for it.
+ *
  *   backward, given O_in, LSE_in (whatever the caller passes):
  *   Delta_i = <dO_i, O_in_i>
  *   P_ij    = exp(s_ij - LSE_in_i),  dP_ij = <dO_i, v_j>
@@ -68,11 +73,20 @@ typedef struct {
   const uint8_t* token_mask;
   const double* sink; /* [Hq] or NULL for "no sink" */
   double scale;
+  const int64_t* seqlen_q; /* [B] valid query rows per batch, or NULL (= Sq) */
+  const int64_t* seqlen_k; /* [B] valid keys per batch, or NULL (= Skv) */
 } om_problem;
+
+/* Valid rows / keys of batch b (lengths outside [0, S] are clamped). */
+static int64_t om_len(const int64_t* len, int64_t b, int64_t S) {
+  if (!len) return S;
+  return len[b] < 0 ? 0 : (len[b] > S ? S : len[b]);
+}
 
 /* Token-level visibility of key j for query i of (b, h). */
 static int om_visible(const om_problem* p, int64_t b, int64_t h, int64_t i,
                       int64_t j) {
+  if (i >= om_len(p->seqlen_q, b, p->Sq) || j >= om_len(p->seqlen_k, b, p->Skv)) return 0;
   switch (p->mask_kind) {
     case OM_MASK_NONE:
       return 1;
@@ -123,6 +137,11 @@ void om_forward_rows(const om_problem* p, const double* q, const double* k,
               b = flat / (p->Sq * p->Hq);
       int64_t c = h / group;
       const double* qi = om_row(q, p->Hq, p->Sq, D, b, h, i);
+      if (i >= om_len(p->seqlen_q, b, p->Sq)) { /* outside the problem */
+        for (int64_t d = 0; d < D; ++d) O_out[r * D + d] = 0.0;
+        LSE_out[r] = INFINITY;
+        continue;
+      }
       double m = -INFINITY;
       for (int64_t j = 0; j < p->Skv; ++j) {
         vis[j] = (uint8_t)om_visible(p, b, h, i, j);
@@ -161,8 +180,11 @@ void om_delta(const om_problem* p, const double* O_in, const double* dO,
               double* delta) {
   const int64_t n = p->B * p->Hq * p->Sq;
 #pragma omp parallel for schedule(static)
-  for (int64_t r = 0; r < n; ++r)
-    delta[r] = om_dot(dO + r * p->D, O_in + r * p->D, p->D);
+  for (int64_t r = 0; r < n; ++r) {
+    const int64_t i = r % p->Sq, b = r / (p->Sq * p->Hq);
+    delta[r] = i < om_len(p->seqlen_q, b, p->Sq) ? om_dot(dO + r * p->D, O_in + r * p->D, p->D)
+                                                  : 0.0;
+  }
 }
 
 /*
@@ -242,7 +264,7 @@ void om_dsink(const om_problem* p, const double* LSE_in, const double* delta,
     double acc = 0.0;
     if (p->sink) {
       for (int64_t b = 0; b < p->B; ++b)
-        for (int64_t i = 0; i < p->Sq; ++i) {
+        for (int64_t i = 0; i < om_len(p->seqlen_q, b, p->Sq); ++i) {
           int64_t row = (b * p->Hq + h) * p->Sq + i;
           acc += exp(p->sink[h] - LSE_in[row]) * delta[row];
         }

@@ -307,3 +307,60 @@ def test_parity_mode_matches_exact_mode_when_fed_its_own_stats():
     dk, dv = oracle.dkdv_cols(pb, q, k, v, dO, lse, ex["delta"], cols)
     np.testing.assert_array_equal(dk, ex["dk"].reshape(-1, D)[cols])
     np.testing.assert_array_equal(dv, ex["dv"].reshape(-1, D)[cols])
+
+
+@pytest.mark.parametrize("kind", [MASK_NONE, MASK_CAUSAL, MASK_SLIDING, MASK_BLOCK])
+def test_varlen_matches_truncated_sequences(kind):
+    # per-batch lengths: batch b is the problem cut to its first Lq[b] rows and
+    # Lk[b] keys (torch fp64 SDPA on the cut problem, sink as an extra key);
+    # rows and keys past the lengths get zeros and LSE = +inf
+    rng = np.random.default_rng(21 + kind)
+    B, Hq, Hkv, S, D = 4, 4, 2, 37, 16
+    Lq = np.array([0, 1, 17, 37])
+    Lk = Lq.copy() if kind in (MASK_CAUSAL, MASK_SLIDING) else np.array([5, 9, 30, 37])
+    sink = _rand(rng, Hq)
+    pb = _problem(kind, B, Hq, Hkv, S, S, D, sink=sink, window=9, bx=6, by=7, rng=rng)
+    pb.seqlen_q, pb.seqlen_k = Lq, Lk
+    q, k, v = _rand(rng, B, Hq, S, D), _rand(rng, B, Hkv, S, D), _rand(rng, B, Hkv, S, D)
+    dO = _rand(rng, B, Hq, S, D)
+    ours = oracle.backward_exact(pb, q, k, v, dO)
+    dsink = np.zeros(Hq)
+    for b in range(B):
+        lq, lk = int(Lq[b]), int(Lk[b])
+        assert np.all(ours["o"][b, :, lq:] == 0) and np.all(np.isposinf(ours["lse"][b, :, lq:]))
+        assert np.all(ours["dq"][b, :, lq:] == 0)
+        assert np.all(ours["dk"][b, :, lk:] == 0) and np.all(ours["dv"][b, :, lk:] == 0)
+        if lq == 0:
+            assert np.all(ours["dk"][b] == 0) and np.all(ours["dv"][b] == 0)
+            continue
+        cut = _problem(kind, 1, Hq, Hkv, lq, lk, D, sink=sink, window=9, bx=6, by=7, rng=rng,
+                       block_mask=(pb.block_mask[b:b + 1, :, :-(-lq // 6), :-(-lk // 7)]
+                                   if kind == MASK_BLOCK else None))
+        ref = _sdpa_reference(cut, q[b:b + 1, :, :lq], k[b:b + 1, :, :lk], v[b:b + 1, :, :lk],
+                              dO[b:b + 1, :, :lq])
+        for name, got in (("o", ours["o"][b:b + 1, :, :lq]), ("lse", ours["lse"][b:b + 1, :, :lq]),
+                          ("dq", ours["dq"][b:b + 1, :, :lq]), ("dk", ours["dk"][b:b + 1, :, :lk]),
+                          ("dv", ours["dv"][b:b + 1, :, :lk])):
+            np.testing.assert_allclose(got, ref[name], rtol=1e-8, atol=1e-9, err_msg=f"{name} b={b}")
+        dsink += ref["dsink"]
+    np.testing.assert_allclose(ours["dsink"], dsink, rtol=1e-8, atol=1e-9)
+
+
+def test_varlen_backward_ignores_rows_past_the_length():
+    # O, dO and LSE of rows outside the problem may hold anything
+    rng = np.random.default_rng(33)
+    B, Hq, Hkv, S, D = 2, 2, 1, 29, 8
+    pb = _problem(MASK_CAUSAL, B, Hq, Hkv, S, S, D, sink=_rand(rng, Hq), rng=rng)
+    pb.seqlen_q = pb.seqlen_k = np.array([11, 20])
+    q, k, v = _rand(rng, B, Hq, S, D), _rand(rng, B, Hkv, S, D), _rand(rng, B, Hkv, S, D)
+    dO = _rand(rng, B, Hq, S, D)
+    O, lse = oracle.forward(pb, q, k, v)
+    clean = oracle.backward(pb, q, k, v, O, dO, lse)
+    O2, dO2, lse2 = O.copy(), dO.copy(), lse.copy()
+    for b, l in enumerate((11, 20)):
+        O2[b, :, l:] = _rand(rng, Hq, S - l, D)
+        dO2[b, :, l:] = _rand(rng, Hq, S - l, D)
+        lse2[b, :, l:] = -_rand(rng, Hq, S - l) ** 2 - 5.0
+    dirty = oracle.backward(pb, q, k, v, O2, dO2, lse2)
+    for name in ("dq", "dk", "dv", "dsink"):
+        np.testing.assert_array_equal(dirty[name], clean[name], err_msg=name)
