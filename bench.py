@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import subprocess
 import sys
@@ -168,7 +169,10 @@ def gpu_inputs(wl, device):
     q, k, v, dO = (t.to(device) for t in (inp.q, inp.k, inp.v, inp.dO))
     sink = inp.sink.to(device) if inp.sink is not None else None
     bm = inp.block_mask.to(device) if inp.block_mask is not None else None
-    mask = mab.Mask(kind=wl.mask_kind, window=wl.window, bx=wl.bx, by=wl.by, block_mask=bm)
+    lq = inp.seqlen_q.to(device) if inp.seqlen_q is not None else None
+    lk = inp.seqlen_k.to(device) if inp.seqlen_k is not None else None
+    mask = mab.Mask(kind=wl.mask_kind, window=wl.window, bx=wl.bx, by=wl.by, block_mask=bm,
+                    seqlen_q=lq, seqlen_k=lk)
     o, lse = mab.fwd(q, k, v, sink, mask, wl.scale)   # O and LSE from the CUDA forward
     torch.cuda.synchronize()
     return inp, dict(q=q, k=k, v=v, o=o, dO=dO, lse=lse, sink=sink, mask=mask)
@@ -181,7 +185,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(device)
     wl = BY_NAME[args.workload]
     inp, t = gpu_inputs(wl, device)
-    pairs = measure.visible_pairs(wl, inp.block_mask)
+    pairs = measure.visible_pairs(wl, inp.block_mask, inp.seqlen_q, inp.seqlen_k)
     fl = measure.flops(wl, pairs)
     ws = mab.workspace(mab.shape_of(t["q"], t["k"]), t["mask"], device)
     dq, dk, dv = torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"])
@@ -322,7 +326,7 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic",
-        "config": workload_config(wl, pairs, fl),
+        "config": workload_config(wl, pairs, fl, inp),
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic,
@@ -343,7 +347,17 @@ def run_ours(args, rank, world, local):
     return line
 
 
-def workload_config(wl, pairs, fl):
+def workload_config(wl, pairs, fl, inp=None):
+    cfg = _workload_config(wl, pairs, fl)
+    if inp is not None and inp.seqlen_q is not None:
+        cfg["seqlen_q"] = [int(x) for x in inp.seqlen_q]
+        cfg["seqlen_k"] = [int(x) for x in inp.seqlen_k]
+        cfg["varlen"] = (f"per-batch valid lengths, uniform in [{math.ceil(wl.varlen_min * wl.Sq)},"
+                         f" {wl.Sq}], on the padded BHSD layout")
+    return cfg
+
+
+def _workload_config(wl, pairs, fl):
     return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "Sq": wl.Sq,
             "Skv": wl.Skv, "D": wl.D, "mask": MASK_NAMES[wl.mask_kind],
             "window": wl.window or None, "bx": wl.bx if wl.mask_kind == 3 else None,
@@ -365,7 +379,9 @@ def cpu_baseline(wl, inp, fl, budget_s: float = 15.0, seed: int = 0):
                         scale=wl.scale, mask_kind=wl.mask_kind, window=wl.window, bx=wl.bx,
                         by=wl.by,
                         block_mask=None if inp.block_mask is None else inp.block_mask.numpy(),
-                        sink=None if inp.sink is None else inp.sink.double().numpy())
+                        sink=None if inp.sink is None else inp.sink.double().numpy(),
+                        seqlen_q=None if inp.seqlen_q is None else inp.seqlen_q.numpy(),
+                        seqlen_k=None if inp.seqlen_k is None else inp.seqlen_k.numpy())
     q = inp.q.double().numpy()
     k = inp.k.double().numpy()
     v = inp.v.double().numpy()
@@ -407,7 +423,7 @@ def run_reference(args, rank, world):
         return None
     wl = BY_NAME[args.workload]
     inp = make_inputs(wl)
-    pairs = measure.visible_pairs(wl, inp.block_mask)
+    pairs = measure.visible_pairs(wl, inp.block_mask, inp.seqlen_q, inp.seqlen_k)
     fl = measure.flops(wl, pairs)
     per_step = max(2.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup):
@@ -422,7 +438,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(wl, pairs, fl), "cpu_baseline": cpu,
+            "config": workload_config(wl, pairs, fl, inp), "cpu_baseline": cpu,
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 

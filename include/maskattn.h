@@ -84,12 +84,25 @@ typedef struct {
 } attn_shape_t;
 
 /* Mask description.  window is read for ATTN_MASK_SLIDING only; bx, by and
- * block_mask for ATTN_MASK_BLOCK only (block_mask is a device pointer). */
+ * block_mask for ATTN_MASK_BLOCK only (block_mask is a device pointer).
+ *
+ * Variable lengths: seqlen_q and seqlen_k, when not NULL, are device int32
+ * arrays [B] of the valid query rows and keys of each batch element (values
+ * are clamped to [0, Sq] and [0, Skv]); NULL means all rows / keys.  Rows
+ * i >= seqlen_q[b] and keys j >= seqlen_k[b] are outside the problem: no pair
+ * with either is visible (the mask rules count i and j from the start of the
+ * sequence, as without lengths), such a row has O = 0 and LSE = +inf in the
+ * forward, dQ = 0 and no part in dSink in the backward whatever O, dO and LSE
+ * hold there, and such a key has dK = dV = 0.  This is the variable-length
+ * batch on the padded BHSD layout: each sequence starts at row 0 of its batch
+ * element.  4-byte aligned. */
 typedef struct {
   int kind; /* attn_mask_kind_t */
   int window;
   int bx, by;
   const uint8_t* block_mask;
+  const int* seqlen_q; /* device [B] or NULL */
+  const int* seqlen_k; /* device [B] or NULL */
 } attn_mask_desc_t;
 
 /* Workspace bytes needed by attn_fwd and attn_bwd for this shape and mask.

@@ -34,7 +34,8 @@ class attn_shape_t(ctypes.Structure):
 
 class attn_mask_desc_t(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("window", ctypes.c_int), ("bx", ctypes.c_int),
-                ("by", ctypes.c_int), ("block_mask", ctypes.c_void_p)]
+                ("by", ctypes.c_int), ("block_mask", ctypes.c_void_p),
+                ("seqlen_q", ctypes.c_void_p), ("seqlen_k", ctypes.c_void_p)]
 
 
 class AttnError(RuntimeError):
@@ -139,10 +140,17 @@ class Mask:
     bx: int = 1
     by: int = 1
     block_mask: Optional[torch.Tensor] = None   # uint8 [B,Hq,nQB,nKB] on the device
+    seqlen_q: Optional[torch.Tensor] = None     # int32 [B] on the device: valid query rows
+    seqlen_k: Optional[torch.Tensor] = None     # int32 [B] on the device: valid keys
 
     def desc(self) -> attn_mask_desc_t:
-        bm = self.block_mask.data_ptr() if self.block_mask is not None else None
-        return attn_mask_desc_t(self.kind, self.window, self.bx, self.by, bm)
+        def ptr(t):
+            return t.data_ptr() if t is not None else None
+        for t, n in ((self.seqlen_q, "seqlen_q"), (self.seqlen_k, "seqlen_k")):
+            if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
+                raise ValueError(f"{n} must be a contiguous int32 tensor")
+        return attn_mask_desc_t(self.kind, self.window, self.bx, self.by, ptr(self.block_mask),
+                                ptr(self.seqlen_q), ptr(self.seqlen_k))
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -309,7 +317,8 @@ class HostBackward:
             sc.wait_event(self.ev_in[c])
             mask = self.mask
             if mask.block_mask is not None:
-                mask = Mask(mask.kind, mask.window, mask.bx, mask.by, mask.block_mask[:, qs])
+                mask = Mask(mask.kind, mask.window, mask.bx, mask.by, mask.block_mask[:, qs],
+                            mask.seqlen_q, mask.seqlen_k)
             sink = d["sink"][qs] if self.has_sink else None
             dsink = d["dsink"][qs] if self.has_sink else None
             r = attn_bwd(self.cshape, _ptr(d["q"][:, qs]), _ptr(d["k"][:, ks]),

@@ -56,6 +56,8 @@ attn_status_t check_shape_mask(const attn_shape_t* sh, const attn_mask_desc_t* m
     default:
       return ATTN_ERR_INVALID_ARG;
   }
+  if ((mk->seqlen_q && !aligned(mk->seqlen_q, 4)) || (mk->seqlen_k && !aligned(mk->seqlen_k, 4)))
+    return ATTN_ERR_INVALID_ARG;
   if (sh->D != HEAD_DIM) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
@@ -163,6 +165,8 @@ AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const W
   p.status = reinterpret_cast<DevStatus*>(ws + L.status);
   p.timeout_ns = wait_timeout_ns();
   p.test_no_loads = test_no_loads();
+  p.seqlen_q = mk->seqlen_q;
+  p.seqlen_k = mk->seqlen_k;
   return p;
 }
 
@@ -320,7 +324,7 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
     e = launch_preprocess(bf16, o, dO, lse, sink, reinterpret_cast<float*>(w + L.nlse2),
                           reinterpret_cast<float*>(w + L.delta),
                           reinterpret_cast<float*>(w + L.dsink_part), shape->B, shape->Hq,
-                          shape->Sq, d.Sq_pad, st);
+                          shape->Sq, d.Sq_pad, mask->seqlen_q, st);
   }
   if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) {
     ProfScope ps("k_mask_tables", st);

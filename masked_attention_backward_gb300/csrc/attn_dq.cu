@@ -117,20 +117,24 @@ struct Ring {
 struct DqUnit {
   int bh, q0, kvh, h;
   QWalk walk;
+  // VARLEN: the call gave per-batch lengths (otherwise every batch element
+  // has all Sq rows and Skv keys, and none is read)
+  template <bool VARLEN>
   __device__ __forceinline__ void init(const AttnParams& p, int u) {
     const int BH = p.B * p.Hq;
     const int qt = p.nQT_q - 1 - u / BH;
     bh = u % BH;
     h = bh % p.Hq;
-    kvh = (bh / p.Hq) * p.Hkv + h / p.group;
+    const int b = bh / p.Hq;
+    kvh = b * p.Hkv + h / p.group;
     q0 = qt * Q_TILE;
-    walk.init(p, bh, qt);
+    walk.init(p, bh, qt, VARLEN ? len_q(p, b) : p.Sq, VARLEN ? len_k(p, b) : p.Skv);
   }
 };
 
 }  // namespace dq_side
 
-template <bool BF16>
+template <bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(dq_side::NUM_THREADS, 1)
 k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tdO,
      const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
@@ -196,7 +200,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
           break;
         }
         DqUnit un;
-        un.init(p, u);
+        un.template init<VARLEN>(p, u);
         mbar_arrive_expect_tx(qbar, 4 * Q_TILE * 128);
         tma_load_3d(smem_u32(s.Q), &tQ, 0, un.q0, un.bh, qbar);
         tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, un.q0, un.bh, qbar);
@@ -238,7 +242,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         const int u = s.unit;
         if (u < 0) break;
         DqUnit un;
-        un.init(p, u);
+        un.template init<VARLEN>(p, u);
         const int N = un.walk.cnt;
         ok = mbar_wait_warp(smem_u32(&s.bar_qa_full), j & 1, wc, TAG_QA);
         __syncwarp();
@@ -278,7 +282,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         const int u = s.unit;
         if (u < 0) break;
         DqUnit un;
-        un.init(p, u);
+        un.template init<VARLEN>(p, u);
         const int N = un.walk.cnt;
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&s.bar_unit_free));
@@ -354,7 +358,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       const int u = ok ? s.unit : -1;
       if (u < 0) break;
       DqUnit un;
-      un.init(p, u);
+      un.template init<VARLEN>(p, u);
       // Q and dO rows of the unit into TMEM as 16-bit pairs (element 2c in
       // the low half of column c): this warp copies d columns
       // 64 g .. 64 g + 63 of its rows.  Every S / dP MMA of the previous unit
@@ -391,7 +395,10 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       const float nlse2_i = p.nlse2[srow];  // -lse log2(e)
       const float delta_i = p.delta[srow];
       int flo, fhi;  // key sub-tiles that are entirely visible
-      full_range_q(p.mask_kind, p.window, p.Sq, p.Skv, un.q0, &flo, &fhi);
+      // keys past the batch's length are masked here; rows past its length
+      // need no mask: their -lse log2 e is -inf, so their P and dS are 0
+      const int Lk = VARLEN ? len_k(p, un.bh / p.Hq) : 0;
+      full_range_q(p.mask_kind, p.window, p.Sq, VARLEN ? Lk : p.Skv, un.q0, &flo, &fhi);
       for (int n = 0; ok && n < un.walk.cnt; ++n, ++m, rg.next()) {
         const int bf = m & 1, st = rg.st;
         // s_full implies the stage's loads landed; waiting on kv_full as well
@@ -409,7 +416,8 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         const int t = s.step_t[st];
         // warp-uniform: the whole 128 x 64 sub-tile is visible
         const bool full = t >= flo && t <= fhi;
-        const uint32_t vis = full ? 0xffffffffu : vis_query_row(p, un.bh, i, t * Q_SUB + 32 * g);
+        const uint32_t vis = full ? 0xffffffffu : vis_query_row(p, un.bh, i, t * Q_SUB + 32 * g, p.Sq,
+                                                    VARLEN ? Lk : p.Skv);
         tmem_wait_ld_regs(sv);
 #pragma unroll
         for (int c = 0; c < 32; ++c) asm volatile("" : "+f"(dp[c]));
@@ -451,7 +459,9 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
 
 cudaError_t launch_dq(bool bf16, const AttnParams& p, const CUtensorMap& tQ, const CUtensorMap& tdO,
                       const CUtensorMap& tK, const CUtensorMap& tV, void* dq, cudaStream_t st) {
-  auto kern = bf16 ? k_dq<true> : k_dq<false>;
+  const bool varlen = p.seqlen_q != nullptr || p.seqlen_k != nullptr;
+  auto kern = bf16 ? (varlen ? k_dq<true, true> : k_dq<true, false>)
+                   : (varlen ? k_dq<false, true> : k_dq<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dq_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;

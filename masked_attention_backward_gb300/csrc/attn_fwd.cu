@@ -117,17 +117,25 @@ struct Cyc {
 
 // Coordinates of work unit u: heaviest causal query tiles first.
 struct FwdUnit {
-  int bh, q0, kvh, h;
+  int bh, q0, kvh, h, Lq, Lk;  // Lq, Lk: valid rows and keys of the batch
   QWalk walk;
   __device__ __forceinline__ void init(const AttnParams& p, int u) {
     const int BH = p.B * p.Hq;
     const int qt = p.nQT_q - 1 - u / BH;
     bh = u % BH;
     h = bh % p.Hq;
-    kvh = (bh / p.Hq) * p.Hkv + h / p.group;
+    const int b = bh / p.Hq;
+    kvh = b * p.Hkv + h / p.group;
     q0 = qt * Q_TILE;
-    walk.init(p, bh, qt);
+    Lq = len_q(p, b);
+    Lk = len_k(p, b);
+    walk.init(p, bh, qt, Lq, Lk);
   }
+};
+
+// What the epilogue of a finished unit needs of it.
+struct FwdDone {
+  int bh, q0, cnt, Lq;
 };
 
 }  // namespace fwd_side
@@ -315,12 +323,12 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
     // no step) and its LSE, then releases the accumulators and the staging
     // space.  (M, l) of the own group come in; the other group's are taken
     // from shared memory.
-    auto epilogue = [&](int j, const FwdUnit& un, float M, float l, float sink2, bool ok) {
+    auto epilogue = [&](int j, const FwdDone& un, float M, float l, float sink2, bool ok) {
       s.xml[j & 1][grp][rloc][0] = M;
       s.xml[j & 1][grp][rloc][1] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s.bar_xml[sp][j & 1]));
-      const int N = un.walk.cnt;
+      const int N = un.cnt;
       bool have = ok && N > 0;
       if (have) have = mbar_wait(smem_u32(&s.bar_xml[sp][j & 1]), (j >> 1) & 1, wc, TAG_XML);
       if (have) have = mbar_wait(smem_u32(&s.bar_acc_full), j & 1, wc, TAG_ACC);
@@ -371,6 +379,7 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
         for (int c = 0; c < 16; ++c) pk[16 * half + c] = pack2<BF16>(acc[2 * c], acc[2 * c + 1]);
       }
       const int r0 = un.q0 + sp * 32;
+      if (r0 + lane >= un.Lq) lse = INFINITY;  // past the batch's length: outside the problem
       if (grp == 0 && r0 + lane < p.Sq) p.lse_out[(size_t)un.bh * p.Sq + r0 + lane] = lse;
       uint16_t* orow = out + ((size_t)un.bh * p.Sq + r0) * HEAD_DIM + 64 * grp;
       warp_store_rows(stage, pk, orow, min(32, p.Sq - r0));
@@ -386,7 +395,7 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
     int cnt = 0;  // steps of this group so far
     Cyc<STAGES> rg;
     Cyc<NBUF> bc;
-    FwdUnit prev;
+    FwdDone prev{0, 0, 0, 0};
     float prev_M = -INFINITY, prev_l = 0.f, prev_sink2 = -INFINITY;
     int j = 0;
     for (; ok; ++j) {
@@ -427,7 +436,7 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
       const float sink2 = p.sink ? p.sink[un.h] * LOG2E : -INFINITY;
       float M = sink2, l = 0.f;
       int flo, fhi;  // key sub-tiles that are entirely visible
-      full_range_q(p.mask_kind, p.window, p.Sq, p.Skv, un.q0, &flo, &fhi);
+      full_range_q(p.mask_kind, p.window, un.Lq, un.Lk, un.q0, &flo, &fhi);
       int last_bf = 0;       // buffer of this group's previous step of the unit
       uint32_t last_ph = 0;  // and the parity of its use
       for (int n = 0; ok && n < un.walk.cnt; ++n, ++m, rg.next(), bc.next()) {
@@ -449,8 +458,10 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
         const int t = s.step_t[st];
         // warp-uniform: the whole 128 x 64 sub-tile is visible
         const bool full = t >= flo && t <= fhi;
-        const uint32_t vis0 = full ? 0xffffffffu : vis_query_row(p, un.bh, i, t * Q_SUB);
-        const uint32_t vis1 = full ? 0xffffffffu : vis_query_row(p, un.bh, i, t * Q_SUB + 32);
+        const uint32_t vis0 =
+            full ? 0xffffffffu : vis_query_row(p, un.bh, i, t * Q_SUB, un.Lq, un.Lk);
+        const uint32_t vis1 =
+            full ? 0xffffffffu : vis_query_row(p, un.bh, i, t * Q_SUB + 32, un.Lq, un.Lk);
         tmem_wait_ld_regs(sv);
         // row maximum of the visible raw logits (the scale is positive, so
         // it is applied once afterwards); eight partial maxima and sums keep
@@ -525,7 +536,7 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
         last_bf = bf;
         last_ph = bc.ph;
       }
-      prev = un;
+      prev = FwdDone{un.bh, un.q0, un.walk.cnt, un.Lq};
       prev_M = M;
       prev_l = l;
       prev_sink2 = sink2;

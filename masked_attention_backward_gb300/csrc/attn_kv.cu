@@ -123,8 +123,9 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
   const int bc = (int)(blockIdx.x % BHkv);
   const int b = bc / p.Hkv, c = bc % p.Hkv;
   const int k0 = t * KV_TILE;
+  const int Lq = len_q(p, b), Lk = len_k(p, b);  // valid rows and keys of the batch
   KVWalk walk;
-  walk.init(p, b, c, t);
+  walk.init(p, b, c, t, Lq, Lk);
   const int N = walk.total(p);
   WaitCtx wc{p.status, &s.abort_flag, p.timeout_ns};
 
@@ -311,7 +312,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       if (lane == 0) mbar_arrive(smem_u32(bar));
     };
     int flo, fhi;  // query sub-tiles that are entirely visible
-    full_range_kv(p.mask_kind, p.window, p.Sq, p.Skv, k0, &flo, &fhi);
+    full_range_kv(p.mask_kind, p.window, Lq, Lk, k0, &flo, &fhi);
     for (int n = 0; ok && n < N; ++n) {
       const int st = n % STAGES;
       // ---- P^T(n) = exp2(S^T(n) * scale*log2e - lse log2e)
@@ -330,7 +331,8 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       const bool full = r >= flo && r <= fhi;
       const uint32_t vis =
           full ? 0xffffu
-               : vis_key_row(p, b * p.Hq + c * p.group + s.step_hh[st], j, r * KV_SUB + 16 * g);
+               : vis_key_row(p, b * p.Hq + c * p.group + s.step_hh[st], j, r * KV_SUB + 16 * g,
+                             Lq, Lk);
       const float4* l4 = reinterpret_cast<const float4*>(&s.nlse2[st][16 * g]);
       float lv[16];
 #pragma unroll

@@ -57,12 +57,25 @@ struct AttnParams {
   DevStatus* status;
   unsigned long long timeout_ns;
   int test_no_loads;   // test hook: the producers issue no loads (every wait runs out)
+  const int* seqlen_q; // [B] valid query rows per batch, or nullptr (= Sq)
+  const int* seqlen_k; // [B] valid keys per batch, or nullptr (= Skv)
 };
+
+#ifdef __CUDACC__
+// Valid query rows / keys of batch b: the per-batch lengths clamped to
+// [0, Sq] / [0, Skv], or the full lengths.
+__device__ __forceinline__ int len_q(const AttnParams& p, int b) {
+  return p.seqlen_q ? min(max(p.seqlen_q[b], 0), p.Sq) : p.Sq;
+}
+__device__ __forceinline__ int len_k(const AttnParams& p, int b) {
+  return p.seqlen_k ? min(max(p.seqlen_k[b], 0), p.Skv) : p.Skv;
+}
+#endif
 
 // ---- launchers (each returns the launch error, if any) ----
 cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const float* lse,
                               const float* sink, float* nlse2, float* delta, float* part, int B,
-                              int Hq, int Sq, int Sq_pad, cudaStream_t st);
+                              int Hq, int Sq, int Sq_pad, const int* seqlen_q, cudaStream_t st);
 cudaError_t launch_dsink_finalize(const float* part, int Hq, int nparts, float* dsink,
                                   cudaStream_t st);
 cudaError_t launch_mask_transpose(const uint8_t* mask, uint8_t* maskT, int BH, int nqb, int nkb,

@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(256)
 k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
              const float* __restrict__ lse, const float* __restrict__ sink,
              float* __restrict__ nlse2, float* __restrict__ delta, float* __restrict__ part, int Hq,
-             int Sq, int Sq_pad, int nparts) {
+             int Sq, int Sq_pad, int nparts, const int* __restrict__ seqlen_q) {
   constexpr int ROWS_PER_WARP = PREP_ROWS / 8;  // 16
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, l16 = lane & 15;
@@ -34,12 +34,15 @@ k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
   const int h = bh % Hq, b = bh / Hq;
   const int row0 = blk * PREP_ROWS + warp * ROWS_PER_WARP;
   const size_t head_rows = (size_t)bh * Sq;
+  // rows past the batch's length are outside the problem: treated like the
+  // padding (Delta 0, -lse log2 e = -inf, no dSink term)
+  const int Lq = seqlen_q ? min(max(seqlen_q[b], 0), Sq) : Sq;
 
   uint4 vo[ROWS_PER_WARP / 2], vd[ROWS_PER_WARP / 2];
 #pragma unroll
   for (int it = 0; it < ROWS_PER_WARP / 2; ++it) {
     int row = row0 + it * 2 + half;
-    if (row < Sq) {
+    if (row < Lq) {
       size_t idx = (head_rows + row) * 16 + l16;
       vo[it] = __ldg(O + idx);
       vd[it] = __ldg(dO + idx);
@@ -66,7 +69,7 @@ k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
     int row = row0 + it * 2 + half;
     if (l16 == 0) {
       size_t o = (size_t)bh * Sq_pad + row;
-      if (row < Sq) {
+      if (row < Lq) {
         float l2 = lse[head_rows + row] * LOG2E;
         delta[o] = acc;
         nlse2[o] = -l2;
@@ -181,15 +184,15 @@ __global__ void k_build_sel(AttnParams p, int* __restrict__ sel_k, int* __restri
 
 cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const float* lse,
                               const float* sink, float* nlse2, float* delta, float* part, int B,
-                              int Hq, int Sq, int Sq_pad, cudaStream_t st) {
+                              int Hq, int Sq, int Sq_pad, const int* seqlen_q, cudaStream_t st) {
   dim3 grid(Sq_pad / PREP_ROWS, B * Hq);
   int nparts = B * (Sq_pad / PREP_ROWS);
   if (bf16)
     k_preprocess<true><<<grid, 256, 0, st>>>((const uint4*)O, (const uint4*)dO, lse, sink, nlse2,
-                                              delta, part, Hq, Sq, Sq_pad, nparts);
+                                              delta, part, Hq, Sq, Sq_pad, nparts, seqlen_q);
   else
     k_preprocess<false><<<grid, 256, 0, st>>>((const uint4*)O, (const uint4*)dO, lse, sink, nlse2,
-                                               delta, part, Hq, Sq, Sq_pad, nparts);
+                                               delta, part, Hq, Sq, Sq_pad, nparts, seqlen_q);
   return cudaGetLastError();
 }
 

@@ -16,10 +16,12 @@ __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
   return upper & ~((1u << lo) - 1u);
 }
 
-// Query row i against keys j0 .. j0+31 (bit c <-> key j0 + c).
-__device__ __forceinline__ uint32_t vis_query_row(const AttnParams& p, int bh, int i, int j0) {
-  if (i >= p.Sq) return 0u;
-  uint32_t inrange = bit_range(0, p.Skv - 1 - j0);
+// Query row i against keys j0 .. j0+31 (bit c <-> key j0 + c); Lq, Lk are
+// the valid rows and keys of the row's batch.
+__device__ __forceinline__ uint32_t vis_query_row(const AttnParams& p, int bh, int i, int j0,
+                                                  int Lq, int Lk) {
+  if (i >= Lq) return 0u;
+  uint32_t inrange = bit_range(0, Lk - 1 - j0);
   switch (p.mask_kind) {
     case MK_NONE:
       return inrange;
@@ -29,7 +31,7 @@ __device__ __forceinline__ uint32_t vis_query_row(const AttnParams& p, int bh, i
       return inrange & bit_range(i - p.window + 1 - j0, i - j0);
     default: {
       const uint8_t* row = p.mask + ((size_t)bh * p.nqb + i / p.bx) * p.nkb;
-      int jend = min(j0 + 31, p.Skv - 1);
+      int jend = min(j0 + 31, Lk - 1);
       if (jend < j0) return 0u;
       uint32_t m = 0;
       for (int kb = j0 / p.by; kb * p.by <= jend; ++kb)
@@ -39,10 +41,12 @@ __device__ __forceinline__ uint32_t vis_query_row(const AttnParams& p, int bh, i
   }
 }
 
-// Key row j against queries i0 .. i0+31 (bit c <-> query i0 + c).
-__device__ __forceinline__ uint32_t vis_key_row(const AttnParams& p, int bh, int j, int i0) {
-  if (j >= p.Skv) return 0u;
-  uint32_t inrange = bit_range(0, p.Sq - 1 - i0);
+// Key row j against queries i0 .. i0+31 (bit c <-> query i0 + c); Lq, Lk
+// are the valid rows and keys of the batch.
+__device__ __forceinline__ uint32_t vis_key_row(const AttnParams& p, int bh, int j, int i0,
+                                                int Lq, int Lk) {
+  if (j >= Lk) return 0u;
+  uint32_t inrange = bit_range(0, Lq - 1 - i0);
   switch (p.mask_kind) {
     case MK_NONE:
       return inrange;
@@ -52,7 +56,7 @@ __device__ __forceinline__ uint32_t vis_key_row(const AttnParams& p, int bh, int
       return inrange & bit_range(j - i0, j + p.window - 1 - i0);
     default: {
       const uint8_t* row = p.maskT + ((size_t)bh * p.nkb + j / p.by) * p.nqb;
-      int iend = min(i0 + 31, p.Sq - 1);
+      int iend = min(i0 + 31, Lq - 1);
       if (iend < i0) return 0u;
       uint32_t m = 0;
       for (int qb = i0 / p.bx; qb * p.bx <= iend; ++qb)
@@ -126,12 +130,17 @@ __host__ __device__ inline void full_range_q(int kind, int window, int Sq, int S
 }
 
 // Walk of a query-tile CTA (Q_TILE rows of head bh) over key sub-tiles of
-// Q_SUB rows.
+// Q_SUB rows; Lq, Lk are the valid rows and keys of the batch (a tile that
+// starts past Lq walks nothing).
 struct QWalk {
   int lo, cnt;
   const int* list;  // select-table row, or nullptr for the closed form
-  __device__ __forceinline__ void init(const AttnParams& p, int bh, int qt) {
-    if (p.mask_kind == MK_BLOCK) {
+  __device__ __forceinline__ void init(const AttnParams& p, int bh, int qt, int Lq, int Lk) {
+    if (qt * Q_TILE >= Lq || Lk <= 0) {
+      lo = 0;
+      cnt = 0;
+      list = nullptr;
+    } else if (p.mask_kind == MK_BLOCK) {
       size_t row = (size_t)bh * p.nQT_q + qt;
       list = p.sel_q + row * p.nKT_q;
       cnt = p.cnt_q[row];
@@ -139,8 +148,7 @@ struct QWalk {
     } else {
       int hi;
       int q0 = qt * Q_TILE;
-      partner_range(p.mask_kind, p.window, true, q0, min(q0 + Q_TILE, p.Sq), Q_SUB, p.Skv, &lo,
-                    &hi);
+      partner_range(p.mask_kind, p.window, true, q0, min(q0 + Q_TILE, Lq), Q_SUB, Lk, &lo, &hi);
       cnt = hi - lo + 1;
       if (cnt < 0) cnt = 0;
       list = nullptr;
@@ -150,26 +158,31 @@ struct QWalk {
 };
 
 // Walk of a key-tile CTA (KV_TILE rows of kv head (b, c)) over (query head of
-// the group, query sub-tile of KV_SUB rows) pairs, head-major.
+// the group, query sub-tile of KV_SUB rows) pairs, head-major; Lq, Lk are the
+// valid rows and keys of batch b (a tile that starts past Lk walks nothing).
 struct KVWalk {
   int lo, cnt_closed;
   int b, c, t;
-  __device__ __forceinline__ void init(const AttnParams& p, int b_, int c_, int t_) {
+  bool none;
+  __device__ __forceinline__ void init(const AttnParams& p, int b_, int c_, int t_, int Lq,
+                                       int Lk) {
     b = b_;
     c = c_;
     t = t_;
     lo = 0;
     cnt_closed = 0;
-    if (p.mask_kind != MK_BLOCK) {
+    const int k0 = t * KV_TILE;
+    none = k0 >= Lk || Lq <= 0;
+    if (!none && p.mask_kind != MK_BLOCK) {
       int hi;
-      int k0 = t * KV_TILE;
-      partner_range(p.mask_kind, p.window, false, k0, min(k0 + KV_TILE, p.Skv), KV_SUB, p.Sq, &lo,
+      partner_range(p.mask_kind, p.window, false, k0, min(k0 + KV_TILE, Lk), KV_SUB, Lq, &lo,
                     &hi);
       cnt_closed = hi - lo + 1;
       if (cnt_closed < 0) cnt_closed = 0;
     }
   }
   __device__ __forceinline__ int count(const AttnParams& p, int hh) const {
+    if (none) return 0;
     if (p.mask_kind != MK_BLOCK) return cnt_closed;
     int bh = b * p.Hq + c * p.group + hh;
     return p.cnt_k[(size_t)bh * p.nKT_k + t];
@@ -180,6 +193,7 @@ struct KVWalk {
     return p.sel_k[((size_t)bh * p.nKT_k + t) * p.nQT_k + idx];
   }
   __device__ __forceinline__ int total(const AttnParams& p) const {
+    if (none) return 0;
     if (p.mask_kind != MK_BLOCK) return cnt_closed * p.group;
     int s = 0;
     for (int hh = 0; hh < p.group; ++hh) s += count(p, hh);

@@ -17,12 +17,29 @@ import numpy as np
 from .workloads import MASK_BLOCK, MASK_CAUSAL, MASK_NONE, MASK_SLIDING, Workload
 
 
-def visible_pairs(wl: Workload, block_mask=None) -> int:
+def visible_pairs(wl: Workload, block_mask=None, seqlen_q=None, seqlen_k=None) -> int:
+    if seqlen_q is not None or seqlen_k is not None:
+        # one batch element at a time, cut to its valid rows and keys
+        lq = [wl.Sq] * wl.B if seqlen_q is None else [int(x) for x in seqlen_q]
+        lk = [wl.Skv] * wl.B if seqlen_k is None else [int(x) for x in seqlen_k]
+        total = 0
+        for b in range(wl.B):
+            Lq, Lk = max(0, min(lq[b], wl.Sq)), max(0, min(lk[b], wl.Skv))
+            if Lq == 0 or Lk == 0:
+                continue
+            cut = wl.with_(B=1, Sq=Lq, Skv=Lk, varlen=False)
+            bm = None
+            if block_mask is not None:
+                bm = np.asarray(block_mask.cpu().numpy() if hasattr(block_mask, "cpu")
+                                else block_mask)[b:b + 1, :, :cut.nqb, :cut.nkb]
+            total += visible_pairs(cut, bm)
+        return total
     heads = wl.B * wl.Hq
     S = wl.Sq
     if wl.mask_kind == MASK_NONE:
         return heads * wl.Sq * wl.Skv
     if wl.mask_kind == MASK_CAUSAL:
+        assert wl.Sq == wl.Skv
         return heads * S * (S + 1) // 2
     if wl.mask_kind == MASK_SLIDING:
         W = wl.window

@@ -8,7 +8,10 @@ Recipe (one ``torch.Generator('cpu')`` per workload, seeded with the workload's
 seed): draw q, k, v, dO as float32 N(0,1) in that order and round them to the
 workload's dtype (round to nearest even); then the per-head sink logits as
 float32 N(0,1) when the workload has a sink; then the random numbers of the
-block mask.
+block mask; then, for a variable-length workload, the valid query rows of
+each batch element, uniform integers in [ceil(varlen_min * Sq), Sq], and the
+valid keys the same way (the query lengths again under a causal or sliding
+mask, where each element is one self-attention sequence).
 
 The five named workloads mirror the mask families and sizes of the pages'
 suites: GQA with a sink and a causal sliding window (tilelang-ascend PR #1
@@ -46,6 +49,8 @@ class Workload:
     density: float = 0.0      # Bernoulli rate of the "random" pattern
     sink: bool = False
     seed: int = 0
+    varlen: bool = False      # per-batch valid lengths (the padded variable-length batch)
+    varlen_min: float = 0.0   # shortest length as a fraction of S
 
     @property
     def scale(self) -> float:
@@ -80,13 +85,20 @@ WORKLOADS = [
     Workload("gqa_sink_causal_s16384", "bf16", B=1, Hq=64, Hkv=8, Sq=16384, Skv=16384,
              mask_kind=MASK_CAUSAL, sink=True, seed=4),
 ]
+# Variable-length GQA-sink backward: 8 sequences of 256..2048 tokens, 64 query
+# heads in groups of 16 (tilelang-ascend examples table, "GQA Sink Backward
+# VarLen": batch 8, heads 64, groups 16, sequence 2048, dim 128, fp16).
+VARLEN_WORKLOADS = [
+    Workload("gqa_sink_varlen_causal_b8_s2048", "f16", B=8, Hq=64, Hkv=4, Sq=2048, Skv=2048,
+             mask_kind=MASK_CAUSAL, sink=True, seed=6, varlen=True, varlen_min=0.125),
+]
 # A smaller member of the causal GQA-sink family (inputs still larger than L2),
 # used for detailed hardware-counter captures.
 PROFILE_WORKLOADS = [
     Workload("gqa_sink_causal_s16384_h16", "bf16", B=1, Hq=16, Hkv=2, Sq=16384, Skv=16384,
              mask_kind=MASK_CAUSAL, sink=True, seed=5),
 ]
-BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_WORKLOADS}
+BY_NAME = {w.name: w for w in WORKLOADS + PROFILE_WORKLOADS + VARLEN_WORKLOADS}
 
 
 @dataclass
@@ -99,6 +111,8 @@ class Inputs:
     sink: Optional[torch.Tensor]          # float32 [Hq] or None
     block_mask: Optional[torch.Tensor]    # uint8 [B,Hq,nQB,nKB] or None
     extra: dict = field(default_factory=dict)
+    seqlen_q: Optional[torch.Tensor] = None   # int32 [B]: valid query rows, or None
+    seqlen_k: Optional[torch.Tensor] = None   # int32 [B]: valid keys, or None
 
 
 def _normal(gen, shape, dtype):
@@ -156,4 +170,13 @@ def make_inputs(wl: Workload, seed: Optional[int] = None) -> Inputs:
     dO = _normal(gen, (wl.B, wl.Hq, wl.Sq, wl.D), dt)
     sink = torch.randn((wl.Hq,), generator=gen, dtype=torch.float32) if wl.sink else None
     bm = _block_mask(wl, gen) if wl.mask_kind == MASK_BLOCK else None
-    return Inputs(wl, q, k, v, dO, sink, bm)
+    lq = lk = None
+    if wl.varlen:
+        lq = torch.randint(math.ceil(wl.varlen_min * wl.Sq), wl.Sq + 1, (wl.B,), generator=gen,
+                           dtype=torch.int32)
+        if wl.mask_kind in (MASK_CAUSAL, MASK_SLIDING):
+            lk = lq.clone()
+        else:
+            lk = torch.randint(math.ceil(wl.varlen_min * wl.Skv), wl.Skv + 1, (wl.B,),
+                               generator=gen, dtype=torch.int32)
+    return Inputs(wl, q, k, v, dO, sink, bm, seqlen_q=lq, seqlen_k=lk)

@@ -27,12 +27,17 @@ def oracle_problem(wl: Workload, inp: Inputs) -> oracle.Problem:
         B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, Sq=wl.Sq, Skv=wl.Skv, D=wl.D, scale=wl.scale,
         mask_kind=wl.mask_kind, window=wl.window, bx=wl.bx, by=wl.by,
         block_mask=None if inp.block_mask is None else inp.block_mask.numpy(),
-        sink=None if inp.sink is None else inp.sink.double().numpy())
+        sink=None if inp.sink is None else inp.sink.double().numpy(),
+        seqlen_q=None if inp.seqlen_q is None else inp.seqlen_q.numpy(),
+        seqlen_k=None if inp.seqlen_k is None else inp.seqlen_k.numpy())
 
 
 def gpu_mask(wl: Workload, inp: Inputs, device="cuda") -> mab.Mask:
     bm = inp.block_mask.to(device) if inp.block_mask is not None else None
-    return mab.Mask(kind=wl.mask_kind, window=wl.window, bx=wl.bx, by=wl.by, block_mask=bm)
+    lq = inp.seqlen_q.to(device) if inp.seqlen_q is not None else None
+    lk = inp.seqlen_k.to(device) if inp.seqlen_k is not None else None
+    return mab.Mask(kind=wl.mask_kind, window=wl.window, bx=wl.bx, by=wl.by, block_mask=bm,
+                    seqlen_q=lq, seqlen_k=lk)
 
 
 def forward_stats(wl: Workload, inp: Inputs, pb=None):

@@ -51,6 +51,9 @@ def test_status_strings(lib):
     (_shape(dtype=5), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
     (_shape(B=1024, Hq=128, Hkv=128), mab.attn_mask_desc_t(0, 0, 1, 1, None),
      mab.ATTN_ERR_INVALID_ARG),
+    # per-batch length arrays must be 4-byte aligned
+    (_shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None, 4098, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None, None, 4097), mab.ATTN_ERR_INVALID_ARG),
 ])
 def test_workspace_size_validation(lib, shape, mask, want):
     r, _ = mab.attn_workspace_size(shape, mask)
@@ -107,11 +110,21 @@ def test_visible_pair_count_matches_oracle():
              Workload("s2", "f16", 1, 2, 2, 5, 5, 8, mask_kind=2, window=9),
              Workload("n", "f16", 1, 2, 1, 13, 29, 8, mask_kind=0),
              Workload("b", "f16", 2, 2, 2, 50, 70, 8, mask_kind=3, bx=6, by=9,
-                      block_pattern="random", density=0.4, seed=3)]
+                      block_pattern="random", density=0.4, seed=3),
+             # variable lengths (lengths 0 .. S drawn by the workload generator)
+             Workload("cv", "f16", 5, 3, 1, 37, 37, 8, mask_kind=1, varlen=True, seed=4),
+             Workload("sv", "f16", 4, 2, 2, 41, 41, 8, mask_kind=2, window=6, varlen=True,
+                      seed=5),
+             Workload("nv", "f16", 4, 2, 1, 13, 29, 8, mask_kind=0, varlen=True, seed=6),
+             Workload("bv", "f16", 4, 2, 2, 50, 70, 8, mask_kind=3, bx=6, by=9,
+                      block_pattern="random", density=0.4, varlen=True, seed=7)]
     for wl in cases:
         inp = make_inputs(wl)
         pb = oracle.Problem(B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, Sq=wl.Sq, Skv=wl.Skv, D=wl.D,
                             scale=wl.scale, mask_kind=wl.mask_kind, window=wl.window, bx=wl.bx,
                             by=wl.by, block_mask=None if inp.block_mask is None
-                            else inp.block_mask.numpy())
-        assert measure.visible_pairs(wl, inp.block_mask) == oracle.count_visible(pb), wl.name
+                            else inp.block_mask.numpy(),
+                            seqlen_q=None if inp.seqlen_q is None else inp.seqlen_q.numpy(),
+                            seqlen_k=None if inp.seqlen_k is None else inp.seqlen_k.numpy())
+        assert (measure.visible_pairs(wl, inp.block_mask, inp.seqlen_q, inp.seqlen_k)
+                == oracle.count_visible(pb)), wl.name
