@@ -92,8 +92,9 @@ typedef struct {
  * i >= seqlen_q[b] and keys j >= seqlen_k[b] are outside the problem: no pair
  * with either is visible (the mask rules count i and j from the start of the
  * sequence, as without lengths), such a row has O = 0 and LSE = +inf in the
- * forward, dQ = 0 and no part in dSink in the backward whatever O, dO and LSE
- * hold there, and such a key has dK = dV = 0.  This is the variable-length
+ * forward, dQ = 0 and no part in dSink in the backward whatever finite values
+ * q, O, dO and LSE hold there, and such a key has dK = dV = 0 whatever finite
+ * values k and v hold there.  This is the variable-length
  * batch on the padded BHSD layout: each sequence starts at row 0 of its batch
  * element.  4-byte aligned. */
 typedef struct {
