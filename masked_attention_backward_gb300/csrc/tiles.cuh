@@ -66,25 +66,6 @@ __device__ __forceinline__ uint32_t vis_key_row(const AttnParams& p, int bh, int
   }
 }
 
-// True when every pair (i, j) with i in [i0, i0 + ni), j in [j0, j0 + nj) is
-// in range and visible under a closed-form mask (never for block masks,
-// whose tiles take the per-thread bitmask path).  Lets a whole sub-tile skip
-// the per-element visibility select.
-__device__ __forceinline__ bool tile_all_visible(const AttnParams& p, int i0, int ni, int j0,
-                                                 int nj) {
-  if (i0 + ni > p.Sq || j0 + nj > p.Skv) return false;
-  switch (p.mask_kind) {
-    case MK_NONE:
-      return true;
-    case MK_CAUSAL:
-      return i0 >= j0 + nj - 1;
-    case MK_SLIDING:
-      return i0 >= j0 + nj - 1 && (i0 + ni - 1) - j0 < p.window;
-    default:
-      return false;
-  }
-}
-
 // The sub-tiles of a walk that are entirely visible form one contiguous
 // range [lo, hi] of partner tile indices under the closed-form masks (empty,
 // hi < lo, for block masks, whose tiles always take the per-element path).
