@@ -201,11 +201,17 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         }
         DqUnit un;
         un.template init<VARLEN>(p, u);
-        mbar_arrive_expect_tx(qbar, 4 * Q_TILE * 128);
-        tma_load_3d(smem_u32(s.Q), &tQ, 0, un.q0, un.bh, qbar);
-        tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, un.q0, un.bh, qbar);
-        tma_load_3d(smem_u32(s.dO), &tdO, 0, un.q0, un.bh, qbar);
-        tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, un.q0, un.bh, qbar);
+        if (un.walk.cnt == 0) {
+          // nothing to contract: the unit's rows only get zeros, so its
+          // Q / dO tiles are not loaded
+          mbar_arrive(qbar);
+        } else {
+          mbar_arrive_expect_tx(qbar, 4 * Q_TILE * 128);
+          tma_load_3d(smem_u32(s.Q), &tQ, 0, un.q0, un.bh, qbar);
+          tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, un.q0, un.bh, qbar);
+          tma_load_3d(smem_u32(s.dO), &tdO, 0, un.q0, un.bh, qbar);
+          tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, un.q0, un.bh, qbar);
+        }
         for (int n = 0; n < un.walk.cnt; ++n, ++m, rg.next()) {
           const int st = rg.st;
           if (m >= STAGES &&

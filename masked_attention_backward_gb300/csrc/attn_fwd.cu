@@ -210,9 +210,15 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
         }
         FwdUnit un;
         un.init(p, u);
-        mbar_arrive_expect_tx(qbar, 2 * Q_TILE * 128);
-        tma_load_3d(smem_u32(s.Q), &tQ, 0, un.q0, un.bh, qbar);
-        tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, un.q0, un.bh, qbar);
+        if (un.walk.cnt == 0) {
+          // nothing to contract: the unit's rows only get O = 0, so its Q
+          // tile is not loaded
+          mbar_arrive(qbar);
+        } else {
+          mbar_arrive_expect_tx(qbar, 2 * Q_TILE * 128);
+          tma_load_3d(smem_u32(s.Q), &tQ, 0, un.q0, un.bh, qbar);
+          tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, un.q0, un.bh, qbar);
+        }
         for (int n = 0; n < un.walk.cnt; ++n, ++m, rg.next()) {
           const int st = rg.i;
           if (m >= STAGES &&

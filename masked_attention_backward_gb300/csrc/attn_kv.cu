@@ -166,12 +166,16 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       tma_prefetch_desc(&tdO);
       tma_prefetch_desc(&tK);
       tma_prefetch_desc(&tV);
+      // a key tile without any step only gets zeros: K and V are not loaded
+      // (and no warp waits for them)
       const uint32_t kvbar = smem_u32(&s.bar_kv_full);
-      mbar_arrive_expect_tx(kvbar, 4 * KV_TILE * 128);
-      tma_load_3d(smem_u32(s.K), &tK, 0, k0, bc, kvbar);
-      tma_load_3d(smem_u32(s.K + KV_TILE * 128), &tK, 64, k0, bc, kvbar);
-      tma_load_3d(smem_u32(s.V), &tV, 0, k0, bc, kvbar);
-      tma_load_3d(smem_u32(s.V + KV_TILE * 128), &tV, 64, k0, bc, kvbar);
+      if (N > 0) {
+        mbar_arrive_expect_tx(kvbar, 4 * KV_TILE * 128);
+        tma_load_3d(smem_u32(s.K), &tK, 0, k0, bc, kvbar);
+        tma_load_3d(smem_u32(s.K + KV_TILE * 128), &tK, 64, k0, bc, kvbar);
+        tma_load_3d(smem_u32(s.V), &tV, 0, k0, bc, kvbar);
+        tma_load_3d(smem_u32(s.V + KV_TILE * 128), &tV, 64, k0, bc, kvbar);
+      }
       KVCursor cur;
       cur.start(p, walk);
       for (int n = 0; n < N; ++n) {
@@ -283,8 +287,9 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     const int rloc = sp * 32 + lane;
     const int j = k0 + rloc;
     const uint32_t lane_base = tbase + ((uint32_t)(sp * 32) << 16);
-    bool ok = mbar_wait(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV);
-    if (ok) {
+    bool ok = true;
+    if (N > 0) ok = mbar_wait(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV);
+    if (ok && N > 0) {
       // K rows into TMEM as 16-bit pairs (element 2c in the low half of column
       // c): this warp copies d columns 32 g .. 32 g + 31 of its rows.
       const int u0 = (g & 1) * 4;
