@@ -206,14 +206,14 @@ def run_ours(args, rank, world, local):
     if status != mab.ATTN_OK:
         raise RuntimeError("device status after warm-up: " + mab.attn_status_string(status))
 
-    # ---- device-timed steps, per-kernel events from the library
-    mab.attn_profile_enable(True)
+    # ---- device-timed steps (the library's per-kernel events stay off here:
+    # they would sit between the kernels and keep dQ from starting on the SMs
+    # that the dK/dV grid's last CTAs leave idle)
     clocks = ClockSampler(local).start()
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    step_ms, kern = [], {}
-    launches = 0
+    step_ms = []
     for _ in range(args.steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -222,15 +222,25 @@ def run_ours(args, rank, world, local):
         e1.record(stream)
         e1.synchronize()
         step_ms.append(e0.elapsed_time(e1))
-        prof = mab.attn_profile_read()
-        launches += len(prof)
-        for name, ms in prof:
-            kern.setdefault(name, []).append(ms)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
+
+    # ---- per-kernel breakdown: a separate pass with the library's events on
+    mab.attn_profile_enable(True)
+    kern = {}
+    per_step_launches = 0
+    for _ in range(min(args.steps, 20)):
+        flush.zero_()
+        step()
+        torch.cuda.synchronize()
+        prof = mab.attn_profile_read()
+        per_step_launches = len(prof)
+        for name, ms in prof:
+            kern.setdefault(name, []).append(ms)
     mab.attn_profile_enable(False)
+    launches = per_step_launches * args.steps  # our kernels in the timed region
     status = mab.device_status(ws)
     if status != mab.ATTN_OK:
         raise RuntimeError("device status after timing: " + mab.attn_status_string(status))

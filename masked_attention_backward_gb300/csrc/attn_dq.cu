@@ -461,6 +461,9 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  // launched to overlap the dK/dV grid's tail: this grid completes only after
+  // that one has, so whatever follows on the stream sees both complete
+  grid_dependency_wait();
 }
 
 cudaError_t launch_dq(bool bf16, const AttnParams& p, const CUtensorMap& tQ, const CUtensorMap& tdO,
@@ -476,10 +479,19 @@ cudaError_t launch_dq(bool bf16, const AttnParams& p, const CUtensorMap& tQ, con
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const int units = p.nQT_q * p.B * p.Hq;
-  dim3 grid((unsigned)(units < sms ? units : sms));
-  kern<<<grid, dq_side::NUM_THREADS, dq_side::SMEM_BYTES, st>>>(tQ, tdO, tK, tV, (uint16_t*)dq,
-                                                                 p);
-  return cudaGetLastError();
+  // programmatic stream serialization: the grid may start while the dK/dV
+  // grid before it finishes (this one reads none of that grid's outputs)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(units < sms ? units : sms));
+  cfg.blockDim = dim3(dq_side::NUM_THREADS);
+  cfg.dynamicSmemBytes = dq_side::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tQ, tdO, tK, tV, (uint16_t*)dq, p);
 }
 
 }  // namespace mab

@@ -158,6 +158,9 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
+  // the dQ kernel that follows needs nothing from this one: it may start on
+  // the SMs this grid's last CTAs leave idle
+  grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

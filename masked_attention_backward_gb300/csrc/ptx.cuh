@@ -322,6 +322,19 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Programmatic dependent launch: lets the grid that follows this one on the
+// stream, launched with programmatic stream serialization, start once every
+// CTA of this grid has executed this (or exited).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grid this one programmatically depends on has completed and
+// its memory operations are visible (returns at once without such a grid).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // max of three floats in one instruction
 __device__ __forceinline__ float fmax3f(float a, float b, float c) {
   float r;
