@@ -461,9 +461,11 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
-  // launched to overlap the dK/dV grid's tail: this grid completes only after
-  // that one has, so whatever follows on the stream sees both complete
-  grid_dependency_wait();
+  // launched to overlap the dK/dV grid's tail: one thread of one CTA keeps
+  // this grid from completing before that one has, so whatever follows on the
+  // stream sees both complete, while every other CTA frees its SM at once
+  // (for kernels of other streams too)
+  if (blockIdx.x == 0 && threadIdx.x == 0) grid_dependency_wait();
 }
 
 cudaError_t launch_dq(bool bf16, const AttnParams& p, const CUtensorMap& tQ, const CUtensorMap& tdO,
