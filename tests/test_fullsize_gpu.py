@@ -5,6 +5,10 @@ the benchmark times (one attn_bwd call over the whole problem).
   dk, dv, dsink against the oracle (parity mode: oracle O and LSE fed to both).
 * blocksparse_random30_s8192: oracle O and LSE for all rows; dq on sampled
   rows and dk, dv on sampled key rows, computed one by one by the oracle.
+* gqa_sink_varlen_causal_b8_s2048: oracle O and LSE for all rows, against
+  which every element of the CUDA forward is compared too; dq on sampled rows,
+  dk, dv on sampled key rows, dsink of every head; exact zeros and +inf past
+  each sequence's length.
 * gqa_sink_causal_s16384: O and LSE from the CUDA forward (the oracle's full
   forward at this size would take minutes), compared against the oracle in
   exact mode (its own fp64 statistics): dq on sampled rows of every head; dk,
@@ -102,3 +106,37 @@ def test_fullsize_causal_16k_sampled(cuda_lib):
     got = dv.double().sum(dim=2)
     err = (got - want).abs().max().item()
     assert err <= 2e-2 * (1 + want.abs().max().item()), err
+
+
+def test_fullsize_varlen_sampled(cuda_lib):
+    wl = BY_NAME["gqa_sink_varlen_causal_b8_s2048"]
+    inp = make_inputs(wl)
+    pb = oracle_problem(wl, inp)
+    O, lse = forward_stats(wl, inp, pb)
+    dev = "cuda"
+    q_d, k_d, v_d = (t.to(dev) for t in (inp.q, inp.k, inp.v))
+    o_g, lse_g = mab.fwd(q_d, k_d, v_d, inp.sink.to(dev), gpu_mask(wl, inp, dev), wl.scale)
+    torch.cuda.synchronize()
+    compare("o", o_g, O.double().numpy(), wl.dtype)
+    g = lse_g.double().cpu().numpy()
+    r = lse.double().numpy()
+    fin = np.isfinite(r)
+    assert np.array_equal(np.isfinite(g), fin)
+    assert np.all(np.abs(g[fin] - r[fin]) <= 1e-4 * (1 + np.abs(r[fin])))
+    run = run_gpu_bwd(wl, inp, O, lse)
+    for b in range(wl.B):
+        L = int(inp.seqlen_q[b])
+        assert torch.all(o_g[b, :, L:].cpu() == 0) and np.all(np.isposinf(g[b, :, L:]))
+        assert torch.all(run.dq[b, :, L:].cpu() == 0)
+        assert torch.all(run.dk[b, :, L:].cpu() == 0) and torch.all(run.dv[b, :, L:].cpu() == 0)
+    rng = np.random.default_rng(0)
+    rows = rng.choice(wl.B * wl.Hq * wl.Sq, size=2048, replace=False)
+    cols = rng.choice(wl.B * wl.Hkv * wl.Skv, size=1024, replace=False)
+    q, k, v, dO = (oracle._f64(t) for t in (inp.q, inp.k, inp.v, inp.dO))
+    dl = oracle.delta(pb, O, dO)
+    dq = oracle.dq_rows(pb, q, k, v, dO, lse, dl, rows)
+    dk, dv = oracle.dkdv_cols(pb, q, k, v, dO, lse, dl, cols)
+    compare("dq", run.dq.reshape(-1, wl.D)[rows], dq, wl.dtype)
+    compare("dk", run.dk.reshape(-1, wl.D)[cols], dk, wl.dtype)
+    compare("dv", run.dv.reshape(-1, wl.D)[cols], dv, wl.dtype)
+    compare("dsink", run.dsink, oracle.dsink(pb, lse, dl), wl.dtype, min_frac=1.0)
