@@ -196,7 +196,7 @@ def run_ours(args, rank, world, local):
 
     def step():
         mab.bwd(t["q"], t["k"], t["v"], t["o"], t["dO"], t["lse"], t["sink"], t["mask"],
-                wl.scale, ws=ws, out=out)
+                wl.scale, ws=ws, out=out, compensated=args.compensated)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -258,7 +258,8 @@ def run_ours(args, rank, world, local):
         host_in["sink"] = t["sink"].cpu().pin_memory() if t["sink"] is not None else None
         host_out = [x.cpu().pin_memory() if x is not None else None for x in out]
         hb = mab.HostBackward(wl.B, wl.Hq, wl.Hkv, wl.Sq, wl.Skv, t["q"].dtype, t["mask"],
-                              wl.scale, t["sink"] is not None, device, chunks=args.e2e_chunks)
+                              wl.scale, t["sink"] is not None, device, chunks=args.e2e_chunks,
+                              compensated=args.compensated)
         h2d, d2h = hb.bytes_per_call(host_in, host_out)
         e2e_ms = []
         for it in range(args.warmup + args.steps):
@@ -336,7 +337,8 @@ def run_ours(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype, "data": "synthetic",
-        "config": workload_config(wl, pairs, fl, inp),
+        "config": dict(workload_config(wl, pairs, fl, inp),
+                       **({"compensated": True} if args.compensated else {})),
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic,
@@ -463,6 +465,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--compensated", action="store_true",
+                    help="time the compensated backward (P and dS as high part + remainder)")
     ap.add_argument("--e2e-chunks", type=int, default=8,
                     help="runs of GQA groups the host-buffer pipeline overlaps")
     args = ap.parse_args()

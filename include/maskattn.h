@@ -77,11 +77,23 @@ typedef enum {
   ATTN_MASK_BLOCK = 3
 } attn_mask_kind_t;
 
-/* Shapes of one call; tensors are contiguous BHSD. */
+/* Shapes of one call; tensors are contiguous BHSD.  flags: 0 or
+ * ATTN_FLAG_COMPENSATED. */
 typedef struct {
   int B, Hq, Hkv, Sq, Skv, D;
   int dtype; /* attn_dtype_t */
+  int flags; /* attn_flag_t bits */
 } attn_shape_t;
+
+/* ATTN_FLAG_COMPENSATED (attn_bwd): P and dS enter the 16-bit contractions
+ * dV += P^T dO, dK += dS^T Q and dQ += dS K as a 16-bit high part plus a
+ * 16-bit remainder (two contractions each), so they are rounded to about 22
+ * bits instead of 11 (fp16) or 8 (bf16) before the fp32 accumulation --
+ * the compensated ("hi + lo") mode for tighter tolerances.  It costs 1.3x
+ * the tensor work and, because the remainders occupy the score buffers
+ * until the accumulations have read them, 1.3x to 1.65x the time.
+ * attn_fwd ignores it. */
+typedef enum { ATTN_FLAG_COMPENSATED = 1 } attn_flag_t;
 
 /* Mask description.  window is read for ATTN_MASK_SLIDING only; bx, by and
  * block_mask for ATTN_MASK_BLOCK only (block_mask is a device pointer).

@@ -29,7 +29,10 @@ EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_bwd_noalloc",
 class attn_shape_t(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
                 ("Sq", ctypes.c_int), ("Skv", ctypes.c_int), ("D", ctypes.c_int),
-                ("dtype", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("flags", ctypes.c_int)]
+
+
+ATTN_FLAG_COMPENSATED = 1
 
 
 class attn_mask_desc_t(ctypes.Structure):
@@ -161,10 +164,10 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
-def shape_of(q: torch.Tensor, k: torch.Tensor) -> attn_shape_t:
+def shape_of(q: torch.Tensor, k: torch.Tensor, flags: int = 0) -> attn_shape_t:
     B, Hq, Sq, D = q.shape
     _, Hkv, Skv, _ = k.shape
-    return attn_shape_t(B, Hq, Hkv, Sq, Skv, D, _dtype_code(q))
+    return attn_shape_t(B, Hq, Hkv, Sq, Skv, D, _dtype_code(q), flags)
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -206,11 +209,12 @@ def fwd(q, k, v, sink, mask: Mask, scale: float, ws: Optional[torch.Tensor] = No
 
 
 def bwd(q, k, v, o, dO, lse, sink, mask: Mask, scale: float, ws: Optional[torch.Tensor] = None,
-        out=None, stream=None):
-    """Backward; returns (dq, dk, dv, dsink) (dsink is None without a sink)."""
+        out=None, stream=None, compensated: bool = False):
+    """Backward; returns (dq, dk, dv, dsink) (dsink is None without a sink).
+    compensated: P and dS enter the contractions as high part + remainder."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (lse, "lse")):
         _check(t, n)
-    shape = shape_of(q, k)
+    shape = shape_of(q, k, ATTN_FLAG_COMPENSATED if compensated else 0)
     if out is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         dsink = torch.empty_like(sink) if sink is not None else None
@@ -252,7 +256,7 @@ class HostBackward:
     whole call."""
 
     def __init__(self, B, Hq, Hkv, Sq, Skv, dtype, mask: Mask, scale: float, has_sink: bool,
-                 device, chunks: int = 8):
+                 device, chunks: int = 8, compensated: bool = False):
         self.B, self.Hq, self.Hkv, self.Sq, self.Skv = B, Hq, Hkv, Sq, Skv
         self.dtype, self.mask, self.scale, self.has_sink = dtype, mask, scale, has_sink
         self.device = torch.device(device)
@@ -275,7 +279,8 @@ class HostBackward:
             self.dev["sink"] = torch.empty(Hq, dtype=torch.float32, device=self.device)
             self.dev["dsink"] = torch.empty(Hq, dtype=torch.float32, device=self.device)
         code = ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16
-        self.cshape = attn_shape_t(B, Hq // chunks, kvc, Sq, Skv, D, code)
+        self.cshape = attn_shape_t(B, Hq // chunks, kvc, Sq, Skv, D, code,
+                                   ATTN_FLAG_COMPENSATED if compensated else 0)
         self.ws = [workspace(self.cshape, mask, self.device) for _ in range(min(3, chunks))]
         self.s_comp = [torch.cuda.Stream(self.device) for _ in range(min(3, chunks))]
         self.s_in = torch.cuda.Stream(self.device)

@@ -37,6 +37,7 @@ attn_status_t check_shape_mask(const attn_shape_t* sh, const attn_mask_desc_t* m
     return ATTN_ERR_INVALID_ARG;
   if (sh->Hq % sh->Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (sh->dtype != ATTN_F16 && sh->dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+  if (sh->flags & ~ATTN_FLAG_COMPENSATED) return ATTN_ERR_INVALID_ARG;
   // sequence lengths up to 2^24 and B*Hq up to 65535 keep every index and
   // grid dimension in range
   if (sh->Sq > (1 << 24) || sh->Skv > (1 << 24) || (long long)sh->B * sh->Hq > 65535)
@@ -165,6 +166,7 @@ AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const W
   p.status = reinterpret_cast<DevStatus*>(ws + L.status);
   p.timeout_ns = wait_timeout_ns();
   p.test_no_loads = test_no_loads();
+  p.compensated = (sh->flags & ATTN_FLAG_COMPENSATED) ? 1 : 0;
   p.seqlen_q = mk->seqlen_q;
   p.seqlen_k = mk->seqlen_k;
   return p;

@@ -134,7 +134,10 @@ struct DqUnit {
 
 }  // namespace dq_side
 
-template <bool BF16, bool VARLEN>
+// HILO: dS enters the dQ contraction as a 16-bit high part (columns
+// 32 g .. 32 g + 15 of group g's slice) plus a 16-bit remainder (columns
+// 32 g + 16 .. 32 g + 31, whose fp32 S values are already in registers).
+template <bool BF16, bool VARLEN, bool HILO>
 __global__ void __launch_bounds__(dq_side::NUM_THREADS, 1)
 k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tdO,
      const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
@@ -303,6 +306,12 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
           for (int kk = 0; kk < Q_SUB / 16; ++kk)
             mma_ts_w(tbase + COL_ACC, a + 32 * (kk >> 1) + 8 * (kk & 1),
                      bK + (uint64_t)((kk * 2048) >> 4), ID_ACC, (n > 0 || kk > 0) ? 1u : 0u);
+          if (HILO) {
+#pragma unroll
+            for (int kk = 0; kk < Q_SUB / 16; ++kk)
+              mma_ts_w(tbase + COL_ACC, a + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
+                       bK + (uint64_t)((kk * 2048) >> 4), ID_ACC, 1u);
+          }
           // S(m) and dP(m) completed before the softmax warps could signal
           // step m, so this commit also frees the K / V stage
           mma_commit_w(smem_u32(&s.bar_kv_empty[st]));
@@ -427,13 +436,21 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         tmem_wait_ld_regs(sv);
 #pragma unroll
         for (int c = 0; c < 32; ++c) asm volatile("" : "+f"(dp[c]));
-        uint32_t pk[16];
+        uint32_t pk[HILO ? 32 : 16];
+        // packs dS of keys 2c, 2c + 1 (and, compensated, the remainder)
+        auto put = [&](int c, float d0, float d1) {
+          pk[c] = pack2<BF16>(d0, d1);
+          if (HILO) {
+            const float2 h = unpack2<BF16>(pk[c]);
+            pk[(HILO ? 16 : 0) + c] = pack2<BF16>(d0 - h.x, d1 - h.y);
+          }
+        };
         if (full) {
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, nlse2_i));
             const float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, nlse2_i));
-            pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
+            put(c, p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
           }
         } else {
 #pragma unroll
@@ -442,10 +459,13 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
             float p1 = fast_exp2(fmaf(sv[2 * c + 1], p.scale_log2, nlse2_i));
             p0 = ((vis >> (2 * c)) & 1u) ? p0 : 0.f;
             p1 = ((vis >> (2 * c + 1)) & 1u) ? p1 : 0.f;
-            pk[c] = pack2<BF16>(p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
+            put(c, p0 * (dp[2 * c] - delta_i), p1 * (dp[2 * c + 1] - delta_i));
           }
         }
-        tmem_st16(lane_base + col, pk);
+        if constexpr (HILO)
+          tmem_st32(lane_base + col, pk);
+        else
+          tmem_st16(lane_base + col, pk);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -471,8 +491,13 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
 cudaError_t launch_dq(bool bf16, const AttnParams& p, const CUtensorMap& tQ, const CUtensorMap& tdO,
                       const CUtensorMap& tK, const CUtensorMap& tV, void* dq, cudaStream_t st) {
   const bool varlen = p.seqlen_q != nullptr || p.seqlen_k != nullptr;
-  auto kern = bf16 ? (varlen ? k_dq<true, true> : k_dq<true, false>)
-                   : (varlen ? k_dq<false, true> : k_dq<false, false>);
+  using Kern = decltype(&k_dq<true, false, false>);
+  static const Kern table[2][2][2] = {
+      {{k_dq<false, false, false>, k_dq<false, false, true>},
+       {k_dq<false, true, false>, k_dq<false, true, true>}},
+      {{k_dq<true, false, false>, k_dq<true, false, true>},
+       {k_dq<true, true, false>, k_dq<true, true, true>}}};
+  const Kern kern = table[bf16 ? 1 : 0][varlen ? 1 : 0][p.compensated ? 1 : 0];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dq_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;

@@ -108,7 +108,11 @@ enum { TAG_KV = 0x201, TAG_KA, TAG_Q_EMPTY, TAG_Q_FULL, TAG_S_FREE, TAG_P_FULL, 
 
 }  // namespace kv_side
 
-template <bool BF16>
+// HILO: P^T and dS^T enter dV and dK as a 16-bit high part (the packed
+// regions) plus a 16-bit remainder, which warp g writes over the first 8 of
+// its own 16 columns of the fp32 S^T / dP^T buffers once it has loaded them;
+// S^T(n + 1) and dP^T(n + 1) then wait for dV(n) / dK(n), which read them.
+template <bool BF16, bool HILO>
 __global__ void __launch_bounds__(kv_side::NUM_THREADS, 1)
 k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tdO,
        const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
@@ -219,7 +223,9 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       // shared memory).  Each waits for the softmax warps to have loaded its
       // previous result.
       const bool is_s = warp == 1;
-      const uint32_t free_bar = smem_u32(is_s ? &s.bar_s_free : &s.bar_dp_free);
+      const uint32_t free_bar =
+          HILO ? smem_u32(is_s ? &s.bar_pt_free : &s.bar_dst_free)
+               : smem_u32(is_s ? &s.bar_s_free : &s.bar_dp_free);
       const uint32_t full_bar = smem_u32(is_s ? &s.bar_s_full : &s.bar_dp_full);
       const uint64_t aV = sdesc_sw128(smem_u32(s.V), 16, 1024);
       bool ok = N == 0 || (is_s ? mbar_wait_warp(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA)
@@ -274,6 +280,12 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         for (int kk = 0; kk < KV_SUB / 16; ++kk)
           mma_ts_w(acc, a + 8 * kk, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC,
                    (n > 0 || kk > 0) ? 1u : 0u);
+        if (HILO) {
+          const uint32_t lo = tbase + (dkside ? COL_DPT : COL_ST);
+#pragma unroll
+          for (int kk = 0; kk < KV_SUB / 16; ++kk)
+            mma_ts_w(acc, lo + 16 * kk, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC, 1u);
+        }
         mma_commit_w(free_bar);
         // S^T(n) and dP^T(n) completed before the softmax warps could write
         // P^T(n) / dS^T(n), so the two commits also free the Q / dO stage
@@ -369,6 +381,14 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         pv[2 * q + 1] = fast_exp2(x.y);
         pk[q] = pack2<BF16>(pv[2 * q], pv[2 * q + 1]);
       }
+      uint32_t pl[HILO ? 8 : 1];  // remainders P - high part
+      if (HILO) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float2 h = unpack2<BF16>(pk[q]);
+          pl[HILO ? q : 0] = pack2<BF16>(pv[2 * q] - h.x, pv[2 * q + 1] - h.y);
+        }
+      }
       // dV(n - 1) must have read P^T(n - 1)
       if (n >= 1 && !mbar_wait(smem_u32(&s.bar_pt_free), (n - 1) & 1, wc, TAG_PT_FREE)) {
         ok = false;
@@ -376,6 +396,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       }
       tc_fence_after();
       tmem_st8(lane_base + COL_PT + 8 * g, pk);
+      if constexpr (HILO) tmem_st8(lane_base + COL_ST + 16 * g, pl);
       tmem_wait_st();
       warp_arrive(&s.bar_p_full);
 
@@ -405,6 +426,10 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
                                 fsub2(make_float2(dp[2 * q], dp[2 * q + 1]),
                                       make_float2(dl[2 * q], dl[2 * q + 1])));
         pk[q] = pack2<BF16>(ds.x, ds.y);
+        if (HILO) {
+          const float2 h = unpack2<BF16>(pk[q]);
+          pl[HILO ? q : 0] = pack2<BF16>(ds.x - h.x, ds.y - h.y);
+        }
       }
       // dK(n - 1) must have read dS^T(n - 1)
       if (n >= 1 && !mbar_wait(smem_u32(&s.bar_dst_free), (n - 1) & 1, wc, TAG_DST_FREE)) {
@@ -413,6 +438,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       }
       tc_fence_after();
       tmem_st8(lane_base + COL_DST + 8 * g, pk);
+      if constexpr (HILO) tmem_st8(lane_base + COL_DPT + 16 * g, pl);
       tmem_wait_st();
       warp_arrive(&s.bar_ds_full);
     }
@@ -456,7 +482,8 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
 cudaError_t launch_dkdv(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                         const CUtensorMap& tdO, const CUtensorMap& tK, const CUtensorMap& tV,
                         void* dk, void* dv, cudaStream_t st) {
-  auto kern = bf16 ? k_dkdv<true> : k_dkdv<false>;
+  auto kern = bf16 ? (p.compensated ? k_dkdv<true, true> : k_dkdv<true, false>)
+                   : (p.compensated ? k_dkdv<false, true> : k_dkdv<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kv_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;

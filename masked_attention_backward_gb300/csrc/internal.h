@@ -57,6 +57,7 @@ struct AttnParams {
   DevStatus* status;
   unsigned long long timeout_ns;
   int test_no_loads;   // test hook: the producers issue no loads (every wait runs out)
+  int compensated;     // backward: P and dS enter the contractions as high part + remainder
   const int* seqlen_q; // [B] valid query rows per batch, or nullptr (= Sq)
   const int* seqlen_k; // [B] valid keys per batch, or nullptr (= Skv)
 };

@@ -73,7 +73,8 @@ class GpuRun:
     ws: torch.Tensor
 
 
-def run_gpu_bwd(wl: Workload, inp: Inputs, O, lse, poison: bool = True) -> GpuRun:
+def run_gpu_bwd(wl: Workload, inp: Inputs, O, lse, poison: bool = True,
+                compensated: bool = False) -> GpuRun:
     dev = "cuda"
     q, k, v, dO = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.dO))
     o, l = O.to(dev), lse.to(dev)
@@ -87,7 +88,8 @@ def run_gpu_bwd(wl: Workload, inp: Inputs, O, lse, poison: bool = True) -> GpuRu
         if dsink is not None:
             dsink.fill_(float("nan"))
     ws = mab.workspace(mab.shape_of(q, k), mask, dev)
-    mab.bwd(q, k, v, o, dO, l, sink, mask, wl.scale, ws=ws, out=(dq, dk, dv, dsink))
+    mab.bwd(q, k, v, o, dO, l, sink, mask, wl.scale, ws=ws, out=(dq, dk, dv, dsink),
+            compensated=compensated)
     torch.cuda.synchronize()
     st = mab.device_status(ws)
     assert st == mab.ATTN_OK, mab.attn_status_string(st)
