@@ -22,8 +22,8 @@ def lib():
     return mab.load()
 
 
-def _shape(B=1, Hq=4, Hkv=2, Sq=256, Skv=256, D=128, dtype=mab.ATTN_BF16):
-    return mab.attn_shape_t(B, Hq, Hkv, Sq, Skv, D, dtype)
+def _shape(B=1, Hq=4, Hkv=2, Sq=256, Skv=256, D=128, dtype=mab.ATTN_BF16, flags=0):
+    return mab.attn_shape_t(B, Hq, Hkv, Sq, Skv, D, dtype, flags)
 
 
 def test_exports_every_declared_symbol(lib):
@@ -49,6 +49,9 @@ def test_status_strings(lib):
     (_shape(), mab.attn_mask_desc_t(3, 0, 0, 16, None), mab.ATTN_ERR_INVALID_ARG),
     (_shape(), mab.attn_mask_desc_t(7, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
     (_shape(dtype=5), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(flags=2), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(flags=-1), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(flags=mab.ATTN_FLAG_COMPENSATED), mab.attn_mask_desc_t(1, 0, 1, 1, None), mab.ATTN_OK),
     (_shape(B=1024, Hq=128, Hkv=128), mab.attn_mask_desc_t(0, 0, 1, 1, None),
      mab.ATTN_ERR_INVALID_ARG),
     # per-batch length arrays must be 4-byte aligned
