@@ -64,6 +64,21 @@ def compare(name: str, got, ref, dtype: str, min_frac: float = MIN_FRAC):
     return rep
 
 
+# The tighter fp16 gate of the GQA-sink backward's precision notes
+# (tilelang-ascend PR #1, Summary): atol 2^-14, rtol 2^-9, at least 99 % of
+# the elements, and no element off by more than 0.1.
+TIGHT_ATOL, TIGHT_RTOL, TIGHT_FRAC, TIGHT_MAX = 2.0 ** -14, 2.0 ** -9, 0.99, 0.1
+
+
+def tight_gate(name: str, got, ref) -> float:
+    g = got.detach().double().cpu().numpy()
+    err = np.abs(g - np.asarray(ref, dtype=np.float64))
+    frac = float((err <= TIGHT_ATOL + TIGHT_RTOL * np.abs(ref)).mean())
+    assert frac >= TIGHT_FRAC, f"{name}: {frac:.5f} of the elements within the tight gate"
+    assert float(err.max()) <= TIGHT_MAX, f"{name}: max error {err.max():.3e}"
+    return frac
+
+
 @dataclass
 class GpuRun:
     dq: torch.Tensor

@@ -112,7 +112,8 @@ def test_bwd_deterministic(cuda_lib):
             assert torch.equal(getattr(a, name), getattr(b, name)), name
 
 
-def test_bwd_more_units_than_sms(cuda_lib):
+@pytest.mark.parametrize("compensated", [False, True], ids=["default", "compensated"])
+def test_bwd_more_units_than_sms(cuda_lib, compensated):
     # 2 x 12 x 11 = 264 query tiles: more than one per SM, so the persistent
     # kernels hand out work units at run time; some tiles see no key at all.
     # Every element against the oracle, and bitwise the same on every run
@@ -124,14 +125,14 @@ def test_bwd_more_units_than_sms(cuda_lib):
     inp.block_mask[1, 7, :, :] = 0      # (1, 7) sees nothing
     pb = oracle_problem(wl, inp)
     O, lse = forward_stats(wl, inp, pb)
-    a = run_gpu_bwd(wl, inp, O, lse)
+    a = run_gpu_bwd(wl, inp, O, lse, compensated=compensated)
     ref = oracle.backward(pb, inp.q, inp.k, inp.v, O, inp.dO, lse)
     for name in ("dq", "dk", "dv"):
         compare(name, getattr(a, name), ref[name], wl.dtype)
     compare("dsink", a.dsink, ref["dsink"], wl.dtype, min_frac=1.0)
     assert torch.all(a.dq[0, 3, 256:512].cpu() == 0) and torch.all(a.dq[1, 7].cpu() == 0)
     for _ in range(2):
-        b = run_gpu_bwd(wl, inp, O, lse)
+        b = run_gpu_bwd(wl, inp, O, lse, compensated=compensated)
         for name in ("dq", "dk", "dv", "dsink"):
             assert torch.equal(getattr(a, name), getattr(b, name)), name
 

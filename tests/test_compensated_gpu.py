@@ -12,21 +12,12 @@ import torch
 
 import oracle
 from masked_attention_backward_gb300.workloads import MASK_CAUSAL, Workload, make_inputs
-from parity import compare, forward_stats, oracle_problem, run_gpu_bwd
+from parity import compare, forward_stats, oracle_problem, run_gpu_bwd, tight_gate
 from test_bwd_gpu import CASES
 
 pytestmark = pytest.mark.gpu
 
 F16 = [w for w in CASES if w.dtype == "f16"]
-
-
-def _tight_gate(name, got, ref):
-    g = got.detach().double().cpu().numpy()
-    err = np.abs(g - ref)
-    frac = float((err <= 6.103515625e-05 + 1.953125e-03 * np.abs(ref)).mean())
-    assert frac >= 0.99, f"{name}: {frac:.5f} of the elements within the tight gate"
-    assert float(err.max()) <= 0.1, f"{name}: max error {err.max():.3e}"
-    return frac
 
 
 @pytest.mark.parametrize("wl", F16, ids=[w.name for w in F16])
@@ -36,7 +27,7 @@ def test_compensated_f16_tight_gate(cuda_lib, wl):
     O, lse = forward_stats(wl, inp, pb)
     run = run_gpu_bwd(wl, inp, O, lse, compensated=True)
     ref = oracle.backward(pb, inp.q, inp.k, inp.v, O, inp.dO, lse)
-    fr = {n: _tight_gate(n, getattr(run, n), ref[n]) for n in ("dq", "dk", "dv")}
+    fr = {n: tight_gate(n, getattr(run, n), ref[n]) for n in ("dq", "dk", "dv")}
     for n in ("dq", "dk", "dv"):
         compare(n, getattr(run, n), ref[n], wl.dtype)
     if inp.sink is not None:

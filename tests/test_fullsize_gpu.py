@@ -23,7 +23,7 @@ import torch
 import oracle
 from masked_attention_backward_gb300 import binding as mab
 from masked_attention_backward_gb300.workloads import BY_NAME, make_inputs
-from parity import compare, forward_stats, gpu_mask, oracle_problem, run_gpu_bwd
+from parity import compare, forward_stats, gpu_mask, oracle_problem, run_gpu_bwd, tight_gate
 
 pytestmark = pytest.mark.gpu
 
@@ -42,12 +42,13 @@ def test_fullsize_every_element(cuda_lib, name):
         compare("dsink", run.dsink, ref["dsink"], wl.dtype, min_frac=1.0)
 
 
-def test_fullsize_blocksparse_random_sampled(cuda_lib):
+@pytest.mark.parametrize("compensated", [False, True], ids=["default", "compensated"])
+def test_fullsize_blocksparse_random_sampled(cuda_lib, compensated):
     wl = BY_NAME["blocksparse_random30_s8192"]
     inp = make_inputs(wl)
     pb = oracle_problem(wl, inp)
     O, lse = forward_stats(wl, inp, pb)
-    run = run_gpu_bwd(wl, inp, O, lse)
+    run = run_gpu_bwd(wl, inp, O, lse, compensated=compensated)
     rng = np.random.default_rng(0)
     rows = rng.choice(wl.B * wl.Hq * wl.Sq, size=2048, replace=False)
     cols = rng.choice(wl.B * wl.Hkv * wl.Skv, size=1024, replace=False)
@@ -58,9 +59,14 @@ def test_fullsize_blocksparse_random_sampled(cuda_lib):
     compare("dq", run.dq.reshape(-1, wl.D)[rows], dq, wl.dtype)
     compare("dk", run.dk.reshape(-1, wl.D)[cols], dk, wl.dtype)
     compare("dv", run.dv.reshape(-1, wl.D)[cols], dv, wl.dtype)
+    if compensated:   # fp16: the tighter gate as well
+        tight_gate("dq", run.dq.reshape(-1, wl.D)[rows], dq)
+        tight_gate("dk", run.dk.reshape(-1, wl.D)[cols], dk)
+        tight_gate("dv", run.dv.reshape(-1, wl.D)[cols], dv)
 
 
-def test_fullsize_causal_16k_sampled(cuda_lib):
+@pytest.mark.parametrize("compensated", [False, True], ids=["default", "compensated"])
+def test_fullsize_causal_16k_sampled(cuda_lib, compensated):
     wl = BY_NAME["gqa_sink_causal_s16384"]
     inp = make_inputs(wl)
     dev = "cuda"
@@ -68,7 +74,8 @@ def test_fullsize_causal_16k_sampled(cuda_lib):
     q, k, v, dO = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.dO))
     sink = inp.sink.to(dev)
     o_gpu, lse_gpu = mab.fwd(q, k, v, sink, mask, wl.scale)
-    dq, dk, dv, dsink = mab.bwd(q, k, v, o_gpu, dO, lse_gpu, sink, mask, wl.scale)
+    dq, dk, dv, dsink = mab.bwd(q, k, v, o_gpu, dO, lse_gpu, sink, mask, wl.scale,
+                                compensated=compensated)
     torch.cuda.synchronize()
     for t in (dq, dk, dv, dsink):
         assert torch.isfinite(t.float()).all()
