@@ -90,9 +90,7 @@ typedef struct {
  * 16-bit remainder (two contractions each), so they are rounded to about 22
  * bits instead of 11 (fp16) or 8 (bf16) before the fp32 accumulation --
  * the compensated ("hi + lo") mode for tighter tolerances.  It costs 1.3x
- * the tensor work and, because the remainders occupy the score buffers
- * until the accumulations have read them, 1.3x to 1.65x the time.
- * attn_fwd ignores it. */
+ * the tensor work and 1.1x to 1.35x the time.  attn_fwd ignores it. */
 typedef enum { ATTN_FLAG_COMPENSATED = 1 } attn_flag_t;
 
 /* Mask description.  window is read for ATTN_MASK_SLIDING only; bx, by and

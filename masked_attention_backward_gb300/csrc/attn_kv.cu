@@ -56,6 +56,8 @@ constexpr int STAGES = 5;      // Q/dO ring depth; the last stage reuses K's til
 constexpr int COL_DV = 0;
 constexpr int COL_DK = 128;
 constexpr int COL_KA = 256;    // K as the A operand (64 columns of 16-bit pairs)
+constexpr int COL_PLO = 256;   // compensated mode: P^T remainders (K stays in shared memory)
+constexpr int COL_DSLO = 288;  // compensated mode: dS^T remainders
 constexpr int COL_ST = 320;    // S^T, fp32
 constexpr int COL_DPT = 384;   // dP^T, fp32
 constexpr int COL_PT = 448;    // P^T, 16-bit pairs
@@ -109,15 +111,17 @@ enum { TAG_KV = 0x201, TAG_KA, TAG_Q_EMPTY, TAG_Q_FULL, TAG_S_FREE, TAG_P_FULL, 
 }  // namespace kv_side
 
 // HILO: P^T and dS^T enter dV and dK as a 16-bit high part (the packed
-// regions) plus a 16-bit remainder, which warp g writes over the first 8 of
-// its own 16 columns of the fp32 S^T / dP^T buffers once it has loaded them;
-// S^T(n + 1) and dP^T(n + 1) then wait for dV(n) / dK(n), which read them.
+// regions) plus a 16-bit remainder, packed the same way into the 64 columns
+// that otherwise hold K: K stays in shared memory (S^T is then issued with
+// both operands there, as dP^T is), so its tile is not a Q/dO stage and the
+// ring has one stage fewer.
 template <bool BF16, bool HILO>
 __global__ void __launch_bounds__(kv_side::NUM_THREADS, 1)
 k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tdO,
        const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
        uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, const AttnParams p) {
   using namespace kv_side;
+  constexpr int NST = HILO ? STAGES - 1 : STAGES;  // Q/dO ring length
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -186,13 +190,14 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       KVCursor cur;
       cur.start(p, walk);
       for (int n = 0; n < N; ++n) {
-        const int st = n % STAGES;
-        if (n >= STAGES &&
-            !mbar_wait(smem_u32(&s.bar_q_empty[st]), ((n / STAGES) - 1) & 1, wc, TAG_Q_EMPTY))
+        const int st = n % NST;
+        if (n >= NST &&
+            !mbar_wait(smem_u32(&s.bar_q_empty[st]), ((n / NST) - 1) & 1, wc, TAG_Q_EMPTY))
           break;
         // the last stage overwrites K's tile: wait until every softmax warp
         // has copied K into TMEM
-        if (n == STAGES - 1 && !mbar_wait(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA)) break;
+        if (!HILO && n == STAGES - 1 && !mbar_wait(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA))
+          break;
         const int r = walk.tile(p, cur.hh, cur.idx);
         const int bh = b * p.Hq + c * p.group + cur.hh;
         // the step's coordinates for the softmax warps, published by the
@@ -223,27 +228,35 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       // shared memory).  Each waits for the softmax warps to have loaded its
       // previous result.
       const bool is_s = warp == 1;
-      const uint32_t free_bar =
-          HILO ? smem_u32(is_s ? &s.bar_pt_free : &s.bar_dst_free)
-               : smem_u32(is_s ? &s.bar_s_free : &s.bar_dp_free);
+      const uint32_t free_bar = smem_u32(is_s ? &s.bar_s_free : &s.bar_dp_free);
       const uint32_t full_bar = smem_u32(is_s ? &s.bar_s_full : &s.bar_dp_full);
       const uint64_t aV = sdesc_sw128(smem_u32(s.V), 16, 1024);
-      bool ok = N == 0 || (is_s ? mbar_wait_warp(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA)
-                                : mbar_wait_warp(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV));
+      const uint64_t aK = sdesc_sw128(smem_u32(s.K), 16, 1024);
+      bool ok = N == 0 || (is_s && !HILO ? mbar_wait_warp(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA)
+                                         : mbar_wait_warp(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV));
       for (int m = 0; ok && m < N; ++m) {
-        const int st = m % STAGES;
-        ok = mbar_wait_warp(smem_u32(&s.bar_q_full[st]), (m / STAGES) & 1, wc, TAG_Q_FULL);
+        const int st = m % NST;
+        ok = mbar_wait_warp(smem_u32(&s.bar_q_full[st]), (m / NST) & 1, wc, TAG_Q_FULL);
         if (ok && m >= 1)
           ok = mbar_wait_warp(free_bar, (m - 1) & 1, wc, is_s ? TAG_S_FREE : TAG_DP_FREE);
         if (!ok) break;
         tc_fence_after();
         if (is_s) {
           const uint64_t bQ = sdesc_sw128(smem_u32(stage_q(s, st)), 16, 1024);
+          if constexpr (HILO) {
 #pragma unroll
-          for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-            mma_ts_w(tbase + COL_ST, tbase + COL_KA + 8 * kk,
-                     bQ + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                     kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+              mma_ss_w(tbase + COL_ST,
+                       aK + (uint64_t)(((kk >> 2) * (KV_TILE * 128) + (kk & 3) * 32) >> 4),
+                       bQ + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                       kk > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+              mma_ts_w(tbase + COL_ST, tbase + COL_KA + 8 * kk,
+                       bQ + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                       kk > 0 ? 1u : 0u);
+          }
         } else {
           const uint64_t bO = sdesc_sw128(smem_u32(stage_do(s, st)), 16, 1024);
 #pragma unroll
@@ -270,7 +283,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       const uint32_t free_bar = smem_u32(dkside ? &s.bar_dst_free : &s.bar_pt_free);
       bool ok = true;
       for (int n = 0; ok && n < N; ++n) {
-        const int st = n % STAGES;
+        const int st = n % NST;
         ok = mbar_wait_warp(full_bar, n & 1, wc, dkside ? TAG_DS_FULL : TAG_P_FULL);
         if (!ok) break;
         tc_fence_after();
@@ -281,10 +294,10 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
           mma_ts_w(acc, a + 8 * kk, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC,
                    (n > 0 || kk > 0) ? 1u : 0u);
         if (HILO) {
-          const uint32_t lo = tbase + (dkside ? COL_DPT : COL_ST);
+          const uint32_t lo = tbase + (dkside ? COL_DSLO : COL_PLO);
 #pragma unroll
           for (int kk = 0; kk < KV_SUB / 16; ++kk)
-            mma_ts_w(acc, lo + 16 * kk, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC, 1u);
+            mma_ts_w(acc, lo + 8 * kk, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC, 1u);
         }
         mma_commit_w(free_bar);
         // S^T(n) and dP^T(n) completed before the softmax warps could write
@@ -304,7 +317,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     const uint32_t lane_base = tbase + ((uint32_t)(sp * 32) << 16);
     bool ok = true;
     if (N > 0) ok = mbar_wait(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV);
-    if (ok && N > 0) {
+    if (!HILO && ok && N > 0) {
       // K rows into TMEM as 16-bit pairs (element 2c in the low half of column
       // c): this warp copies d columns 32 g .. 32 g + 31 of its rows.
       const int u0 = (g & 1) * 4;
@@ -334,12 +347,12 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     int flo, fhi;  // query sub-tiles that are entirely visible
     full_range_kv(p.mask_kind, p.window, Lq, Lk, k0, &flo, &fhi);
     for (int n = 0; ok && n < N; ++n) {
-      const int st = n % STAGES;
+      const int st = n % NST;
       // ---- P^T(n) = exp2(S^T(n) * scale*log2e - lse log2e)
       // s_full implies the stage's loads landed; waiting on q_full as well
       // makes the bulk-copied -lse log2e / Delta rows visible to this thread
       if (!mbar_wait(smem_u32(&s.bar_s_full), n & 1, wc, TAG_S_FULL) ||
-          !mbar_wait(smem_u32(&s.bar_q_full[st]), (n / STAGES) & 1, wc, TAG_Q_FULL)) {
+          !mbar_wait(smem_u32(&s.bar_q_full[st]), (n / NST) & 1, wc, TAG_Q_FULL)) {
         ok = false;
         break;
       }
@@ -396,7 +409,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       }
       tc_fence_after();
       tmem_st8(lane_base + COL_PT + 8 * g, pk);
-      if constexpr (HILO) tmem_st8(lane_base + COL_ST + 16 * g, pl);
+      if constexpr (HILO) tmem_st8(lane_base + COL_PLO + 8 * g, pl);
       tmem_wait_st();
       warp_arrive(&s.bar_p_full);
 
@@ -438,7 +451,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       }
       tc_fence_after();
       tmem_st8(lane_base + COL_DST + 8 * g, pk);
-      if constexpr (HILO) tmem_st8(lane_base + COL_DPT + 16 * g, pl);
+      if constexpr (HILO) tmem_st8(lane_base + COL_DSLO + 8 * g, pl);
       tmem_wait_st();
       warp_arrive(&s.bar_ds_full);
     }
