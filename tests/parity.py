@@ -64,10 +64,26 @@ def compare(name: str, got, ref, dtype: str, min_frac: float = MIN_FRAC):
     return rep
 
 
-# The tighter fp16 gate of the GQA-sink backward's precision notes
-# (tilelang-ascend PR #1, Summary): atol 2^-14, rtol 2^-9, at least 99 % of
-# the elements, and no element off by more than 0.1.
-TIGHT_ATOL, TIGHT_RTOL, TIGHT_FRAC, TIGHT_MAX = 2.0 ** -14, 2.0 ** -9, 0.99, 0.1
+def load_gate(path=None) -> dict:
+    """The fp16 precision gate printed for the GQA-sink backward example's
+    test suite (tests/golden/fp16_precision_gate.txt, with its citation)."""
+    import os
+    path = path or os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                                "fp16_precision_gate.txt")
+    gate = {}
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if len(line) == 2:
+                gate[line[0]] = float(line[1])
+    return gate
+
+
+# The page prints atol and rtol to three figures; they are read as 2^-14 and
+# 2^-9 (6.1035e-5, 1.9531e-3), which tests/test_golden.py checks.
+_GATE = load_gate()
+TIGHT_ATOL, TIGHT_RTOL = 2.0 ** -14, 2.0 ** -9
+TIGHT_FRAC, TIGHT_MAX = _GATE["required_ratio"], _GATE["max_abs_limit"]
 
 
 def tight_gate(name: str, got, ref) -> float:
