@@ -438,6 +438,7 @@ def run_reference(args, rank, world):
     pairs = measure.visible_pairs(wl, inp.block_mask, inp.seqlen_q, inp.seqlen_k)
     fl = measure.flops(wl, pairs)
     per_step = max(2.0, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    per_step = min(per_step, args.cpu_seconds)   # --cpu-seconds bounds each sample
     for i in range(args.warmup):
         cpu_baseline(wl, inp, fl, budget_s=per_step / 4, seed=100 + i)
     ests = [cpu_baseline(wl, inp, fl, budget_s=per_step, seed=i) for i in range(args.steps)]
