@@ -77,6 +77,7 @@ struct __align__(1024) Smem {
   uint8_t K[STAGES][2 * Q_SUB * 128];
   uint8_t V[STAGES][2 * Q_SUB * 128];
   int step_t[STAGES];           // key sub-tile of the step in the stage
+  uint32_t step_vis[STAGES];    // aligned block masks: bit 2 sp + g = region (sp, g) visible
   int unit;                     // unit of the latest Q / dO load, -1: none left
   uint64_t bar_q_full;          // Q, dO of the unit landed in shared memory
   uint64_t bar_qa_full;         // Q, dO copied into TMEM (all softmax warps)
@@ -148,6 +149,11 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
                                      ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int U = p.nQT_q * p.B * p.Hq;
+  // a block mask whose blocks hold whole softmax-warp regions (32 queries x
+  // 32 keys): each region is visible entirely or not at all (with per-batch
+  // lengths the per-element path is kept, which spares that instance's registers)
+  const bool blk_regions =
+      !VARLEN && p.mask_kind == MK_BLOCK && (p.bx & 31) == 0 && (p.by & 31) == 0;
   WaitCtx wc{p.status, &s.abort_flag, p.timeout_ns};
 
   if (threadIdx.x == 0) {
@@ -217,14 +223,38 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         }
         for (int n = 0; n < un.walk.cnt; ++n, ++m, rg.next()) {
           const int st = rg.st;
+          const int t = un.walk.tile(n);
+          // aligned block masks: the mask byte of each softmax warp's 32-query
+          // x 32-key region, loaded before the wait below (which hides the
+          // latency; indices clamped into the mask, ranges applied after)
+          uint32_t mv[8];
+          if (blk_regions) {
+            const uint8_t* mb = p.mask + (size_t)un.bh * p.nqb * p.nkb;
+#pragma unroll
+            for (int sp2 = 0; sp2 < 4; ++sp2) {
+              const int qb = min((un.q0 + 32 * sp2) / p.bx, p.nqb - 1);
+#pragma unroll
+              for (int g2 = 0; g2 < 2; ++g2) {
+                const int kb = min((t * Q_SUB + 32 * g2) / p.by, p.nkb - 1);
+                mv[2 * sp2 + g2] = mb[(size_t)qb * p.nkb + kb];
+              }
+            }
+          }
           if (m >= STAGES &&
               !mbar_wait(smem_u32(&s.bar_kv_empty[st]), rg.ph ^ 1u, wc,
                          TAG_KV_EMPTY)) {
             ok = false;
             break;
           }
-          const int t = un.walk.tile(n);
           s.step_t[st] = t;  // published by the arrive below together with the loads
+          if (blk_regions) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (mv[e] && un.q0 + 32 * (e >> 1) < p.Sq && t * Q_SUB + 32 * (e & 1) < p.Skv)
+                w |= 1u << e;
+            s.step_vis[st] = w;
+          }
           const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
           mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
           tma_load_3d(smem_u32(s.K[st]), &tK, 0, t * Q_SUB, un.kvh, fb);
@@ -431,8 +461,16 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         const int t = s.step_t[st];
         // warp-uniform: the whole 128 x 64 sub-tile is visible
         const bool full = t >= flo && t <= fhi;
-        const uint32_t vis = full ? 0xffffffffu : vis_query_row(p, un.bh, i, t * Q_SUB + 32 * g, p.Sq,
-                                                    VARLEN ? Lk : p.Skv);
+        uint32_t vis;
+        if (full) {
+          vis = 0xffffffffu;
+        } else if (blk_regions) {
+          vis = ((s.step_vis[st] >> (2 * sp + g)) & 1u) && i < p.Sq
+                    ? bit_range(0, (VARLEN ? Lk : p.Skv) - 1 - (t * Q_SUB + 32 * g))
+                    : 0u;
+        } else {
+          vis = vis_query_row(p, un.bh, i, t * Q_SUB + 32 * g, p.Sq, VARLEN ? Lk : p.Skv);
+        }
         tmem_wait_ld_regs(sv);
 #pragma unroll
         for (int c = 0; c < 32; ++c) asm volatile("" : "+f"(dp[c]));

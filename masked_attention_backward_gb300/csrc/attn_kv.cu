@@ -75,6 +75,7 @@ struct __align__(1024) Smem {
   float delta[STAGES][KV_SUB];
   int step_r[STAGES];            // query sub-tile of the step in the stage
   int step_hh[STAGES];           // its query head within the group
+  uint32_t step_vis[STAGES];     // aligned block masks: bit 4 sp + g = region (sp, g) visible
   uint64_t bar_kv_full;          // K, V landed
   uint64_t bar_ka_full;          // K copied into TMEM (all softmax warps)
   uint64_t bar_q_full[STAGES];
@@ -135,6 +136,9 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
   KVWalk walk;
   walk.init(p, b, c, t, Lq, Lk);
   const int N = walk.total(p);
+  // a block mask whose blocks hold whole softmax-warp regions (32 keys x 16
+  // queries): each region is visible entirely or not at all
+  const bool blk_regions = p.mask_kind == MK_BLOCK && (p.by & 31) == 0 && (p.bx & 15) == 0;
   WaitCtx wc{p.status, &s.abort_flag, p.timeout_ns};
 
   if (threadIdx.x == 0) {
@@ -191,6 +195,24 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       cur.start(p, walk);
       for (int n = 0; n < N; ++n) {
         const int st = n % NST;
+        const int r = walk.tile(p, cur.hh, cur.idx);
+        const int bh = b * p.Hq + c * p.group + cur.hh;
+        // aligned block masks: the mask byte of each softmax warp's 32-key x
+        // 16-query region, loaded before the waits below (which hide the
+        // latency; indices clamped into the mask, ranges applied after)
+        uint32_t mv[16];
+        if (blk_regions) {
+          const uint8_t* mt = p.maskT + (size_t)bh * p.nkb * p.nqb;
+#pragma unroll
+          for (int sp2 = 0; sp2 < 4; ++sp2) {
+            const int kb = min((k0 + 32 * sp2) / p.by, p.nkb - 1);
+#pragma unroll
+            for (int g2 = 0; g2 < 4; ++g2) {
+              const int qb = min((r * KV_SUB + 16 * g2) / p.bx, p.nqb - 1);
+              mv[4 * sp2 + g2] = mt[(size_t)kb * p.nqb + qb];
+            }
+          }
+        }
         if (n >= NST &&
             !mbar_wait(smem_u32(&s.bar_q_empty[st]), ((n / NST) - 1) & 1, wc, TAG_Q_EMPTY))
           break;
@@ -198,12 +220,18 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         // has copied K into TMEM
         if (!HILO && n == STAGES - 1 && !mbar_wait(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA))
           break;
-        const int r = walk.tile(p, cur.hh, cur.idx);
-        const int bh = b * p.Hq + c * p.group + cur.hh;
         // the step's coordinates for the softmax warps, published by the
         // arrive below together with the loads
         s.step_r[st] = r;
         s.step_hh[st] = cur.hh;
+        if (blk_regions) {
+          uint32_t w = 0;
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (mv[e] && k0 + 32 * (e >> 2) < p.Skv && r * KV_SUB + 16 * (e & 3) < p.Sq)
+              w |= 1u << e;
+          s.step_vis[st] = w;
+        }
         cur.next(p, walk);
         const uint32_t fb = smem_u32(&s.bar_q_full[st]);
         mbar_arrive_expect_tx(fb, 4 * KV_SUB * 128 + 2 * KV_SUB * 4);
@@ -362,10 +390,17 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       const int r = s.step_r[st];
       // warp-uniform: the whole 64 x 128 sub-tile is visible
       const bool full = r >= flo && r <= fhi;
-      const uint32_t vis =
-          full ? 0xffffu
-               : vis_key_row(p, b * p.Hq + c * p.group + s.step_hh[st], j, r * KV_SUB + 16 * g,
-                             Lq, Lk);
+      uint32_t vis;
+      if (full) {
+        vis = 0xffffu;
+      } else if (blk_regions) {
+        vis = ((s.step_vis[st] >> (4 * sp + g)) & 1u) && j < Lk
+                  ? bit_range(0, Lq - 1 - (r * KV_SUB + 16 * g))
+                  : 0u;
+      } else {
+        vis = vis_key_row(p, b * p.Hq + c * p.group + s.step_hh[st], j, r * KV_SUB + 16 * g, Lq,
+                          Lk);
+      }
       const float4* l4 = reinterpret_cast<const float4*>(&s.nlse2[st][16 * g]);
       float lv[16];
 #pragma unroll
