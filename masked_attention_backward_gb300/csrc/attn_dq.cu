@@ -208,7 +208,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
           mbar_arrive(qbar);
           break;
         }
-        DqUnit un;
+        DqUnit un{};
         un.template init<VARLEN>(p, u);
         if (un.walk.cnt == 0) {
           // nothing to contract: the unit's rows only get zeros, so its
@@ -280,7 +280,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         if (!mbar_wait_warp(smem_u32(&s.bar_q_full), j & 1, wc, TAG_Q)) break;
         const int u = s.unit;
         if (u < 0) break;
-        DqUnit un;
+        DqUnit un{};
         un.template init<VARLEN>(p, u);
         const int N = un.walk.cnt;
         ok = mbar_wait_warp(smem_u32(&s.bar_qa_full), j & 1, wc, TAG_QA);
@@ -320,7 +320,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         if (!mbar_wait_warp(smem_u32(&s.bar_q_full), j & 1, wc, TAG_Q)) break;
         const int u = s.unit;
         if (u < 0) break;
-        DqUnit un;
+        DqUnit un{};
         un.template init<VARLEN>(p, u);
         const int N = un.walk.cnt;
         __syncwarp();
@@ -402,7 +402,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       ok = mbar_wait(smem_u32(&s.bar_q_full), j & 1, wc, TAG_Q);
       const int u = ok ? s.unit : -1;
       if (u < 0) break;
-      DqUnit un;
+      DqUnit un{};
       un.template init<VARLEN>(p, u);
       // Q and dO rows of the unit into TMEM as 16-bit pairs (element 2c in
       // the low half of column c): this warp copies d columns
