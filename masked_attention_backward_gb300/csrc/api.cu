@@ -77,7 +77,7 @@ Dims dims_of(const attn_shape_t* sh, const attn_mask_desc_t* mk) {
   d.nKT_k = (sh->Skv + KV_TILE - 1) / KV_TILE;
   d.nQT_q = (sh->Sq + Q_TILE - 1) / Q_TILE;
   d.nKT_q = (sh->Skv + Q_SUB - 1) / Q_SUB;
-  d.nparts = sh->B * (d.Sq_pad / PREP_ROWS);
+  d.nparts = sh->B * (d.Sq_pad / PREP_BLOCK_ROWS);
   return d;
 }
 

@@ -17,7 +17,8 @@ constexpr int KV_TILE = 128;
 constexpr int KV_SUB = 64;
 constexpr int Q_TILE = 128;
 constexpr int Q_SUB = 64;
-constexpr int PREP_ROWS = 128;  // rows per preprocess block; also the padding unit
+constexpr int PREP_ROWS = 128;  // padding unit of the per-row statistics
+constexpr int PREP_BLOCK_ROWS = 64;  // rows per preprocess block (divides PREP_ROWS)
 constexpr float LOG2E = 1.4426950408889634f;
 
 enum MaskKind { MK_NONE = 0, MK_CAUSAL = 1, MK_SLIDING = 2, MK_BLOCK = 3 };

@@ -18,21 +18,23 @@
 
 namespace mab {
 
-// One block = PREP_ROWS rows of one (b, h).  Each half-warp owns a row: 16
-// lanes x 16 bytes cover the 128-element row of O and of dO, so every warp
-// load is a fully coalesced 512-byte request.
+// One block = PREP_BLOCK_ROWS rows of one (b, h).  Each half-warp owns a row:
+// 16 lanes x 16 bytes cover the 128-element row of O and of dO, so every warp
+// load is a fully coalesced 512-byte request.  A thread holds 4 rows of each
+// in flight; small blocks keep several per SM resident, so that one block's
+// loads are in flight while another reduces and exits.
 template <bool BF16>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)
 k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
              const float* __restrict__ lse, const float* __restrict__ sink,
              float* __restrict__ nlse2, float* __restrict__ delta, float* __restrict__ part, int Hq,
              int Sq, int Sq_pad, int nparts, const int* __restrict__ seqlen_q) {
-  constexpr int ROWS_PER_WARP = PREP_ROWS / 8;  // 16
+  constexpr int ROWS_PER_WARP = PREP_BLOCK_ROWS / 8;  // 8
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, l16 = lane & 15;
   const int blk = blockIdx.x, bh = blockIdx.y;
   const int h = bh % Hq, b = bh / Hq;
-  const int row0 = blk * PREP_ROWS + warp * ROWS_PER_WARP;
+  const int row0 = blk * PREP_BLOCK_ROWS + warp * ROWS_PER_WARP;
   const size_t head_rows = (size_t)bh * Sq;
   // rows past the batch's length are outside the problem: treated like the
   // padding (Delta 0, -lse log2 e = -inf, no dSink term)
@@ -185,8 +187,8 @@ __global__ void k_build_sel(AttnParams p, int* __restrict__ sel_k, int* __restri
 cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const float* lse,
                               const float* sink, float* nlse2, float* delta, float* part, int B,
                               int Hq, int Sq, int Sq_pad, const int* seqlen_q, cudaStream_t st) {
-  dim3 grid(Sq_pad / PREP_ROWS, B * Hq);
-  int nparts = B * (Sq_pad / PREP_ROWS);
+  dim3 grid(Sq_pad / PREP_BLOCK_ROWS, B * Hq);
+  int nparts = B * (Sq_pad / PREP_BLOCK_ROWS);
   if (bf16)
     k_preprocess<true><<<grid, 256, 0, st>>>((const uint4*)O, (const uint4*)dO, lse, sink, nlse2,
                                               delta, part, Hq, Sq, Sq_pad, nparts, seqlen_q);

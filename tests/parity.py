@@ -146,6 +146,7 @@ def full_parity(wl: Workload, seed=None):
 # query tile / key sub-tile of the dQ walk) and the workspace layout that the
 # library carves; mirrored here so that tests can read the device tables.
 KV_TILE, KV_SUB, Q_TILE, Q_SUB, PREP_ROWS = 128, 64, 128, 64, 128
+PREP_BLOCK_ROWS = 64  # rows per preprocess block: one dSink partial each
 
 
 def _a256(x):
@@ -160,7 +161,7 @@ def ws_layout(wl: Workload) -> dict:
     off = _a256(16)
     L["nlse2"] = off; off = _a256(off + BH * Sq_pad * 4)
     L["delta"] = off; off = _a256(off + BH * Sq_pad * 4)
-    L["dsink_part"] = off; off = _a256(off + wl.Hq * wl.B * (Sq_pad // PREP_ROWS) * 4)
+    L["dsink_part"] = off; off = _a256(off + wl.Hq * wl.B * (Sq_pad // PREP_BLOCK_ROWS) * 4)
     d = {"Sq_pad": Sq_pad, "nQT_k": cdiv(wl.Sq, KV_SUB), "nKT_k": cdiv(wl.Skv, KV_TILE),
          "nQT_q": cdiv(wl.Sq, Q_TILE), "nKT_q": cdiv(wl.Skv, Q_SUB)}
     if wl.mask_kind == MASK_BLOCK:
