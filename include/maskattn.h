@@ -154,7 +154,12 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
  * stream capture on the device).  Errors: those of attn_bwd, and
  * ATTN_ERR_WORKSPACE when attn_workspace_size() for the shape exceeds 32 MiB.
  * All calls on a device share the array: calls whose GPU work overlaps in
- * time race on it and give wrong results, so order them on one stream. */
+ * time race on it and give wrong results, so order them on one stream.
+ * `stream` must belong to the current device (ATTN_ERR_INVALID_ARG
+ * otherwise).  The array's address is cached per device for the life of the
+ * process: after cudaDeviceReset on a device this entry point must not be
+ * used on it again.  A device wait that runs out is recorded in the array's
+ * status word: read it with attn_noalloc_get_device_status. */
 attn_status_t attn_bwd_noalloc(const attn_shape_t* shape, const void* q, const void* k,
                                const void* v, const void* o, const void* dO, const float* lse,
                                const float* sink, const attn_mask_desc_t* mask, float scale,
@@ -164,6 +169,13 @@ attn_status_t attn_bwd_noalloc(const attn_shape_t* shape, const void* q, const v
  * used `ws` left in the workspace: ATTN_OK, or ATTN_ERR_TIMEOUT when a device
  * wait ran out.  ATTN_ERR_CUDA if the synchronization itself fails. */
 attn_status_t attn_get_device_status(const void* ws, void* stream);
+
+/* Synchronizes `stream` (which must belong to the current device), then
+ * reads the status word that the last attn_bwd_noalloc call on the current
+ * device left in the library's scratch array: ATTN_OK or ATTN_ERR_TIMEOUT.
+ * ATTN_ERR_INVALID_ARG for a stream of another device, ATTN_ERR_CUDA if the
+ * synchronization or the read fails. */
+attn_status_t attn_noalloc_get_device_status(void* stream);
 
 /* Per-kernel timing, for diagnostics and benchmarks.  attn_profile_enable(1)
  * makes later attn_fwd / attn_bwd calls on this process bracket every kernel

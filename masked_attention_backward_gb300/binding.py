@@ -22,8 +22,8 @@ ATTN_MASK_NONE, ATTN_MASK_CAUSAL, ATTN_MASK_SLIDING, ATTN_MASK_BLOCK = range(4)
 
 # Every symbol include/maskattn.h declares.
 EXPORTS = ("attn_workspace_size", "attn_fwd", "attn_bwd", "attn_bwd_noalloc",
-           "attn_get_device_status", "attn_profile_enable", "attn_profile_read",
-           "attn_status_string")
+           "attn_get_device_status", "attn_noalloc_get_device_status", "attn_profile_enable",
+           "attn_profile_read", "attn_status_string")
 
 
 class attn_shape_t(ctypes.Structure):
@@ -72,6 +72,8 @@ def load(build: bool = True) -> ctypes.CDLL:
             lib.attn_bwd_noalloc.restype = ctypes.c_int
             lib.attn_get_device_status.argtypes = [vp, vp]
             lib.attn_get_device_status.restype = ctypes.c_int
+            lib.attn_noalloc_get_device_status.argtypes = [vp]
+            lib.attn_noalloc_get_device_status.restype = ctypes.c_int
             lib.attn_profile_enable.argtypes = [ctypes.c_int]
             lib.attn_profile_enable.restype = ctypes.c_int
             lib.attn_profile_read.argtypes = [ctypes.POINTER(ctypes.c_char_p),
@@ -117,6 +119,11 @@ def attn_bwd_noalloc(shape, q, k, v, o, dO, lse, sink, mask, scale, dq, dk, dv, 
 
 def attn_get_device_status(ws, stream) -> int:
     return load().attn_get_device_status(ws, stream)
+
+
+def attn_noalloc_get_device_status(stream) -> int:
+    """Status word of the last attn_bwd_noalloc call on the current device."""
+    return load().attn_noalloc_get_device_status(stream)
 
 
 def attn_profile_enable(on: bool) -> int:

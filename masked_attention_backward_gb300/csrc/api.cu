@@ -15,6 +15,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "maskattn.h"
@@ -169,16 +170,23 @@ AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const W
   p.compensated = (sh->flags & ATTN_FLAG_COMPENSATED) ? 1 : 0;
   p.seqlen_q = mk->seqlen_q;
   p.seqlen_k = mk->seqlen_k;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+    p.num_sms = sms;
   return p;
 }
 
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
 // ---- optional per-kernel events (attn_profile_enable) ----
+// The mutex is taken only by calls made while profiling is on (and by the
+// profiling calls themselves): with profiling off, host threads driving other
+// streams or devices enqueue without waiting on one another.
 struct Profiler {
   static constexpr int kMax = 16;
   std::mutex mu;
-  bool on = false;
+  std::atomic<bool> on{false};
   bool created = false;
   int device = -1;
   cudaEvent_t ev[kMax][2];
@@ -187,13 +195,14 @@ struct Profiler {
 };
 Profiler g_prof;
 
-// Brackets one launch with events when profiling is on.
+// Brackets one launch with events when the call is profiled (the caller then
+// holds the profiler's mutex).
 struct ProfScope {
   cudaStream_t st;
   bool active;
   int slot;
-  ProfScope(const char* name, cudaStream_t s) : st(s), active(false), slot(-1) {
-    if (!g_prof.on || !g_prof.created || g_prof.n >= Profiler::kMax) return;
+  ProfScope(bool profiled, const char* name, cudaStream_t s) : st(s), active(false), slot(-1) {
+    if (!profiled || !g_prof.created || g_prof.n >= Profiler::kMax) return;
     slot = g_prof.n++;
     g_prof.names[slot] = name;
     active = cudaEventRecord(g_prof.ev[slot][0], st) == cudaSuccess;
@@ -203,10 +212,17 @@ struct ProfScope {
   }
 };
 
-// Called at the start of every profiled API call.
-void prof_begin() {
-  if (!g_prof.on) return;
-  g_prof.n = 0;
+// Called at the start of every profiled API call, with the mutex held.
+void prof_begin() { g_prof.n = 0; }
+
+// Takes the profiler's mutex only when profiling is on; returns whether this
+// call is profiled.
+bool prof_lock(std::unique_lock<std::mutex>& lock) {
+  if (!g_prof.on.load(std::memory_order_acquire)) return false;
+  lock.lock();
+  if (!g_prof.on.load(std::memory_order_relaxed)) return false;  // switched off meanwhile
+  prof_begin();
+  return true;
 }
 
 // Transposed mask and both select tables (block masks only).
@@ -269,15 +285,15 @@ attn_status_t attn_fwd(const attn_shape_t* shape, const void* q, const void* k, 
       !make_bhsd_map(&tK, k, bf16, BHkv, shape->Skv, Q_SUB) ||
       !make_bhsd_map(&tV, v, bf16, BHkv, shape->Skv, Q_SUB))
     return ATTN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_prof.mu);
-  prof_begin();
+  std::unique_lock<std::mutex> lock(g_prof.mu, std::defer_lock);
+  const bool prof = prof_lock(lock);
   cudaError_t e = cudaMemsetAsync(w + L.status, 0, sizeof(DevStatus), st);
   if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) {
-    ProfScope ps("k_mask_tables", st);
+    ProfScope ps(prof, "k_mask_tables", st);
     e = enqueue_tables(shape, L, w, p, st);
   }
   if (e == cudaSuccess) {
-    ProfScope ps("k_attn_fwd", st);
+    ProfScope ps(prof, "k_attn_fwd", st);
     e = launch_fwd(bf16, p, tQ, tK, tV, o, st);
   }
   return cuda_status(e);
@@ -318,30 +334,30 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
       !make_bhsd_map(&tVs, v, bf16, BHkv, shape->Skv, Q_SUB))
     return ATTN_ERR_CUDA;
 
-  std::lock_guard<std::mutex> lock(g_prof.mu);
-  prof_begin();
+  std::unique_lock<std::mutex> lock(g_prof.mu, std::defer_lock);
+  const bool prof = prof_lock(lock);
   cudaError_t e = cudaMemsetAsync(w + L.status, 0, sizeof(DevStatus), st);
   if (e == cudaSuccess) {
-    ProfScope ps("k_preprocess", st);
+    ProfScope ps(prof, "k_preprocess", st);
     e = launch_preprocess(bf16, o, dO, lse, sink, reinterpret_cast<float*>(w + L.nlse2),
                           reinterpret_cast<float*>(w + L.delta),
                           reinterpret_cast<float*>(w + L.dsink_part), shape->B, shape->Hq,
                           shape->Sq, d.Sq_pad, mask->seqlen_q, st);
   }
   if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) {
-    ProfScope ps("k_mask_tables", st);
+    ProfScope ps(prof, "k_mask_tables", st);
     e = enqueue_tables(shape, L, w, p, st);
   }
   if (e == cudaSuccess) {
-    ProfScope ps("k_dkdv", st);
+    ProfScope ps(prof, "k_dkdv", st);
     e = launch_dkdv(bf16, p, tQs, tdOs, tKt, tVt, dk, dv, st);
   }
   if (e == cudaSuccess) {
-    ProfScope ps("k_dq", st);
+    ProfScope ps(prof, "k_dq", st);
     e = launch_dq(bf16, p, tQt, tdOt, tKs, tVs, dq, st);
   }
   if (e == cudaSuccess && sink) {
-    ProfScope ps("k_dsink_finalize", st);
+    ProfScope ps(prof, "k_dsink_finalize", st);
     e = launch_dsink_finalize(reinterpret_cast<const float*>(w + L.dsink_part), shape->Hq,
                               d.nparts, dsink, st);
   }
@@ -378,7 +394,7 @@ attn_status_t attn_profile_enable(int on) {
       g_prof.device = dev;
     }
   }
-  g_prof.on = on != 0;
+  g_prof.on.store(on != 0, std::memory_order_release);
   g_prof.n = 0;
   return ATTN_OK;
 }

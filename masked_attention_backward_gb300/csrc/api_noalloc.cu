@@ -49,6 +49,17 @@ void* scratch_on_current_device() {
   return g_scratch_ptr[dev];
 }
 
+// True when `stream` belongs to the current device (the legacy default
+// stream, NULL, always does).
+bool stream_on_current_device(void* stream) {
+  if (!stream) return true;
+  int dev = -1, sdev = -2;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaStreamGetDevice(reinterpret_cast<cudaStream_t>(stream), &sdev) != cudaSuccess)
+    return false;
+  return dev == sdev;
+}
+
 }  // namespace
 
 extern "C" attn_status_t attn_bwd_noalloc(const attn_shape_t* shape, const void* q, const void* k,
@@ -60,8 +71,20 @@ extern "C" attn_status_t attn_bwd_noalloc(const attn_shape_t* shape, const void*
   attn_status_t r = attn_workspace_size(shape, mask, &need);
   if (r != ATTN_OK) return r;
   if (need > NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;
+  if (!stream_on_current_device(stream)) return ATTN_ERR_INVALID_ARG;
   void* ws = scratch_on_current_device();
   if (!ws) return ATTN_ERR_CUDA;
   return attn_bwd(shape, q, k, v, o, dO, lse, sink, mask, scale, dq, dk, dv, dsink, ws,
                   NOALLOC_SCRATCH_BYTES, stream);
+}
+
+// The status word of the last attn_bwd_noalloc call on the current device
+// lives at the start of the library's scratch array, which callers cannot
+// address; this reads it back the way attn_get_device_status reads a
+// workspace's.
+extern "C" attn_status_t attn_noalloc_get_device_status(void* stream) {
+  if (!stream_on_current_device(stream)) return ATTN_ERR_INVALID_ARG;
+  void* ws = scratch_on_current_device();
+  if (!ws) return ATTN_ERR_CUDA;
+  return attn_get_device_status(ws, stream);
 }

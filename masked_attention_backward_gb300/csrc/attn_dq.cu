@@ -193,14 +193,17 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       tma_prefetch_desc(&tV);
       bool ok = true;
       int m = 0;  // step counter across units
+      int q_loaded = -1;  // last unit whose Q / dO tiles were loaded
       Ring rg;
       const uint32_t qbar = smem_u32(&s.bar_q_full);
       for (int j = 0; ok; ++j) {
         // the Q / dO tiles and the unit slot are free once every other warp
         // has taken the previous unit (the softmax warps: copied its Q / dO
         // into TMEM and stored the epilogue before it, staged in the Q tile)
-        if (j >= 1 && !mbar_wait(smem_u32(&s.bar_unit_free), (j - 1) & 1, wc, TAG_UNIT_FREE))
+        if (j >= 1 && !mbar_wait(smem_u32(&s.bar_unit_free), (j - 1) & 1, wc, TAG_UNIT_FREE)) {
+          ok = false;
           break;
+        }
         int u = j == 0 ? (int)blockIdx.x : (int)(gridDim.x + atomicAdd(&p.status->next_unit, 1u));
         if (u >= U) u = -1;
         s.unit = u;  // published by the arrive on q_full
@@ -220,6 +223,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
           tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, un.q0, un.bh, qbar);
           tma_load_3d(smem_u32(s.dO), &tdO, 0, un.q0, un.bh, qbar);
           tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, un.q0, un.bh, qbar);
+          q_loaded = j;
         }
         for (int n = 0; n < un.walk.cnt; ++n, ++m, rg.next()) {
           const int st = rg.st;
@@ -262,6 +266,12 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
           tma_load_3d(smem_u32(s.V[st]), &tV, 0, t * Q_SUB, un.kvh, fb);
           tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, t * Q_SUB, un.kvh, fb);
         }
+      }
+      if (!ok) {
+        // the CTA gave up: let the copies still in flight land before it exits
+        if (q_loaded >= 0) mbar_drain(qbar, q_loaded & 1, wc.timeout_ns);
+        for (int k = m > STAGES ? m - STAGES : 0; k < m; ++k)
+          mbar_drain(smem_u32(&s.bar_kv_full[k % STAGES]), (k / STAGES) & 1, wc.timeout_ns);
       }
     }
   } else if (warp >= 1 && warp < SM_WARP0) {
@@ -350,11 +360,11 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         if (ok) mma_commit_w(smem_u32(&s.bar_acc_full));  // the unit's accumulator is complete
       }
     }
-    // this warp's MMAs must be complete before TMEM is freed (also on the
-    // abort path)
+    // this warp's MMAs must be complete before TMEM is freed (also when the
+    // CTA gave up, hence a wait that ignores the abort flag)
     const uint32_t done = smem_u32(&s.bar_x_done[warp - 1]);
     mma_commit_w(done);
-    mbar_wait_warp(done, 0, wc, TAG_X_DONE);
+    mbar_drain_warp(done, 0, wc.timeout_ns);
   } else {
     // ------------------------------------------------------------ softmax warps
     const int sp = warp & 3, g = (warp - SM_WARP0) >> 2;
@@ -366,9 +376,17 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
     // accumulator and the staging space.
     auto epilogue = [&](int j, const DqUnit& un, bool ok) {
       uint32_t pk[32];
-      bool have = ok && mbar_wait(smem_u32(&s.bar_acc_full), j & 1, wc, TAG_ACC);
-      have = have && un.walk.cnt > 0;
+      const bool acc_ok = ok && mbar_wait(smem_u32(&s.bar_acc_full), j & 1, wc, TAG_ACC);
+      const bool have = acc_ok && un.walk.cnt > 0;
       tc_fence_after();
+      const int r0 = un.q0 + sp * 32;
+      uint16_t* orow = dq + ((size_t)un.bh * p.Sq + r0) * HEAD_DIM + 64 * g;
+      if (!__all_sync(0xffffffffu, acc_ok)) {
+        // the CTA gave up: a copy may still be landing in the Q tile, so the
+        // zeros go straight to global memory
+        warp_zero_rows(orow, 64, min(32, p.Sq - r0));
+        return;
+      }
       if (have) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -383,15 +401,15 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
 #pragma unroll
         for (int c = 0; c < 32; ++c) pk[c] = 0u;
       }
-      const int r0 = un.q0 + sp * 32;
-      uint16_t* orow = dq + ((size_t)un.bh * p.Sq + r0) * HEAD_DIM + 64 * g;
-      warp_store_rows(stage, pk, orow, min(32, p.Sq - r0));
-      // the next TMA load into the Q tile comes after this warp's generic
-      // accesses to it
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      // the accumulator is in registers: the next unit's first dQ MMA may
+      // overwrite it while this warp stores the rows
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s.bar_acc_empty));
+      warp_store_rows(stage, pk, orow, min(32, p.Sq - r0));
+      // the next TMA load into the Q tile (after unit_free) comes after this
+      // warp's generic accesses to it
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     };
     bool ok = true;
     int m = 0;  // step counter across units

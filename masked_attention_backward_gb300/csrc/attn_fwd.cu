@@ -193,14 +193,17 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
       tma_prefetch_desc(&tV);
       bool ok = true;
       int m = 0;  // step counter across units
+      int q_loaded = -1;  // last unit whose Q tile was loaded
       Cyc<STAGES> rg;
       const uint32_t qbar = smem_u32(&s.bar_q_full);
       for (int j = 0; ok; ++j) {
         // the Q tile and the unit slot are free once every other warp has
         // taken the previous unit (the softmax warps: copied its Q into TMEM
         // and stored the epilogue before it, staged in the Q tile)
-        if (j >= 1 && !mbar_wait(smem_u32(&s.bar_unit_free), (j - 1) & 1, wc, TAG_UNIT_FREE))
+        if (j >= 1 && !mbar_wait(smem_u32(&s.bar_unit_free), (j - 1) & 1, wc, TAG_UNIT_FREE)) {
+          ok = false;
           break;
+        }
         int u = j == 0 ? (int)blockIdx.x : (int)(gridDim.x + atomicAdd(&p.status->next_unit, 1u));
         if (u >= U) u = -1;
         s.unit = u;  // published by the arrive on q_full
@@ -218,6 +221,7 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
           mbar_arrive_expect_tx(qbar, 2 * Q_TILE * 128);
           tma_load_3d(smem_u32(s.Q), &tQ, 0, un.q0, un.bh, qbar);
           tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, un.q0, un.bh, qbar);
+          q_loaded = j;
         }
         for (int n = 0; n < un.walk.cnt; ++n, ++m, rg.next()) {
           const int st = rg.i;
@@ -235,6 +239,12 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
           tma_load_3d(smem_u32(s.V[st]), &tV, 0, t * Q_SUB, un.kvh, fb);
           tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, t * Q_SUB, un.kvh, fb);
         }
+      }
+      if (!ok) {
+        // the CTA gave up: let the copies still in flight land before it exits
+        if (q_loaded >= 0) mbar_drain(qbar, q_loaded & 1, wc.timeout_ns);
+        for (int k = m > STAGES ? m - STAGES : 0; k < m; ++k)
+          mbar_drain(smem_u32(&s.bar_kv_full[k % STAGES]), (k / STAGES) & 1, wc.timeout_ns);
       }
     }
   } else if (warp < SM_WARP0) {
@@ -312,11 +322,11 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
         if (ok) mma_commit_w(smem_u32(&s.bar_acc_full));  // the unit's accumulators are complete
       }
     }
-    // this warp's MMAs must be complete before TMEM is freed (also on the
-    // abort path)
+    // this warp's MMAs must be complete before TMEM is freed (also when the
+    // CTA gave up, hence a wait that ignores the abort flag)
     const uint32_t done = smem_u32(&s.bar_x_done[warp - 1]);
     mma_commit_w(done);
-    mbar_wait_warp(done, 0, wc, TAG_X_DONE);
+    mbar_drain_warp(done, 0, wc.timeout_ns);
   } else {
     // ------------------------------------------------------------ softmax warps
     const int sp = warp & 3, grp = (warp - SM_WARP0) >> 2;
@@ -388,6 +398,12 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
       if (r0 + lane >= un.Lq) lse = INFINITY;  // past the batch's length: outside the problem
       if (grp == 0 && r0 + lane < p.Sq) p.lse_out[(size_t)un.bh * p.Sq + r0 + lane] = lse;
       uint16_t* orow = out + ((size_t)un.bh * p.Sq + r0) * HEAD_DIM + 64 * grp;
+      if (!__all_sync(0xffffffffu, ok && (N == 0 || have))) {
+        // the CTA gave up: a copy may still be landing in the Q tile, so the
+        // zeros go straight to global memory
+        warp_zero_rows(orow, 64, min(32, p.Sq - r0));
+        return;
+      }
       warp_store_rows(stage, pk, orow, min(32, p.Sq - r0));
       // the next TMA load into the Q tile comes after this warp's generic
       // accesses to it

@@ -161,6 +161,19 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     mbar_init(smem_u32(&s.bar_x_done[1]), 1);
     mbar_init(smem_u32(&s.bar_acc_full), 2);
     fence_mbar_init();
+    // K and V of the tile, loaded while the rest of the CTA sets up (they do
+    // not depend on the kernels before this one); a key tile without any step
+    // only gets zeros: K and V are not loaded (and no warp waits for them)
+    if (N > 0 && !p.test_no_loads) {
+      tma_prefetch_desc(&tK);
+      tma_prefetch_desc(&tV);
+      const uint32_t kvbar = smem_u32(&s.bar_kv_full);
+      mbar_arrive_expect_tx(kvbar, 4 * KV_TILE * 128);
+      tma_load_3d(smem_u32(s.K), &tK, 0, k0, bc, kvbar);
+      tma_load_3d(smem_u32(s.K + KV_TILE * 128), &tK, 64, k0, bc, kvbar);
+      tma_load_3d(smem_u32(s.V), &tV, 0, k0, bc, kvbar);
+      tma_load_3d(smem_u32(s.V + KV_TILE * 128), &tV, 64, k0, bc, kvbar);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&s.tmem_base), 512);
@@ -170,8 +183,12 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
-  // the dQ kernel that follows needs nothing from this one: it may start on
-  // the SMs this grid's last CTAs leave idle
+  // Launched behind the preprocess kernel with programmatic serialization
+  // (closed-form masks), this grid may start before that one has finished:
+  // wait for it before any of its results are read.  Only then let the dQ
+  // kernel that follows start (it needs nothing from this grid, but reads the
+  // preprocess results): it may take the SMs this grid's last CTAs leave idle.
+  grid_dependency_wait();
   grid_launch_dependents();
 
   if (warp == 0) {
@@ -179,24 +196,26 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     if (lane == 0 && !p.test_no_loads) {
       tma_prefetch_desc(&tQ);
       tma_prefetch_desc(&tdO);
-      tma_prefetch_desc(&tK);
-      tma_prefetch_desc(&tV);
-      // a key tile without any step only gets zeros: K and V are not loaded
-      // (and no warp waits for them)
       const uint32_t kvbar = smem_u32(&s.bar_kv_full);
-      if (N > 0) {
-        mbar_arrive_expect_tx(kvbar, 4 * KV_TILE * 128);
-        tma_load_3d(smem_u32(s.K), &tK, 0, k0, bc, kvbar);
-        tma_load_3d(smem_u32(s.K + KV_TILE * 128), &tK, 64, k0, bc, kvbar);
-        tma_load_3d(smem_u32(s.V), &tV, 0, k0, bc, kvbar);
-        tma_load_3d(smem_u32(s.V + KV_TILE * 128), &tV, 64, k0, bc, kvbar);
+      // a short walk ends soon: bring the K / V tile of the CTA that will
+      // likely take this SM next (the grid is dispatched in order, one CTA per
+      // SM) into L2 now, so that its first wait is for L2 rather than HBM
+      const int succ = (int)blockIdx.x + p.num_sms;
+      if (N <= 64 && succ < (int)gridDim.x) {
+        const int t2 = succ / BHkv, bc2 = succ % BHkv;
+        tma_prefetch_l2_3d(&tK, 0, t2 * KV_TILE, bc2);
+        tma_prefetch_l2_3d(&tK, 64, t2 * KV_TILE, bc2);
+        tma_prefetch_l2_3d(&tV, 0, t2 * KV_TILE, bc2);
+        tma_prefetch_l2_3d(&tV, 64, t2 * KV_TILE, bc2);
       }
       KVCursor cur;
       cur.start(p, walk);
+      int issued = 0;  // steps whose loads were issued
       for (int n = 0; n < N; ++n) {
         const int st = n % NST;
-        const int r = walk.tile(p, cur.hh, cur.idx);
-        const int bh = b * p.Hq + c * p.group + cur.hh;
+        int r, hh;
+        kv_step(p, walk, cur, &hh, &r);
+        const int bh = b * p.Hq + c * p.group + hh;
         // aligned block masks: the mask byte of each softmax warp's 32-key x
         // 16-query region, loaded before the waits below (which hide the
         // latency; indices clamped into the mask, ranges applied after)
@@ -223,7 +242,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         // the step's coordinates for the softmax warps, published by the
         // arrive below together with the loads
         s.step_r[st] = r;
-        s.step_hh[st] = cur.hh;
+        s.step_hh[st] = hh;
         if (blk_regions) {
           uint32_t w = 0;
 #pragma unroll
@@ -232,7 +251,6 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
               w |= 1u << e;
           s.step_vis[st] = w;
         }
-        cur.next(p, walk);
         const uint32_t fb = smem_u32(&s.bar_q_full[st]);
         mbar_arrive_expect_tx(fb, 4 * KV_SUB * 128 + 2 * KV_SUB * 4);
         uint8_t* sq = stage_q(s, st);
@@ -244,6 +262,13 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         const size_t srow = (size_t)bh * p.Sq_pad + (size_t)r * KV_SUB;
         bulk_load(smem_u32(s.nlse2[st]), p.nlse2 + srow, KV_SUB * 4, fb);
         bulk_load(smem_u32(s.delta[st]), p.delta + srow, KV_SUB * 4, fb);
+        issued = n + 1;
+      }
+      if (issued < N) {
+        // the CTA gave up: let the copies still in flight land before it exits
+        mbar_drain(kvbar, 0, wc.timeout_ns);
+        for (int n = issued > NST ? issued - NST : 0; n < issued; ++n)
+          mbar_drain(smem_u32(&s.bar_q_full[n % NST]), (n / NST) & 1, wc.timeout_ns);
       }
     }
   } else if (warp >= 1 && warp < SM_WARP0) {
@@ -296,10 +321,11 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         }
         mma_commit_w(full_bar);
       }
-      // this warp's MMAs must be complete before TMEM is freed (abort path)
+      // this warp's MMAs must be complete before TMEM is freed (also when the
+      // CTA gave up, hence a wait that ignores the abort flag)
       const uint32_t done = smem_u32(&s.bar_x_done[is_s ? 0 : 1]);
       mma_commit_w(done);
-      mbar_wait_warp(done, 0, wc, TAG_X_DONE);
+      mbar_drain_warp(done, 0, wc.timeout_ns);
     } else {
       // warp 3: dV += P^T(n) dO; warp 4: dK += dS^T(n) Q (A from the packed
       // regions, B MN-major).  Both commit to q_empty and acc_full, which
@@ -335,7 +361,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       // completes when every MMA of both warps has (also on the abort path,
       // so that TMEM is idle before it is freed)
       mma_commit_w(smem_u32(&s.bar_acc_full));
-      mbar_wait_warp(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
+      mbar_drain_warp(smem_u32(&s.bar_acc_full), 0, wc.timeout_ns);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
@@ -494,14 +520,24 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     bool have = ok && N > 0;
     if (have) have = mbar_wait(smem_u32(&s.bar_acc_full), 0, wc, TAG_ACC);
     tc_fence_after();
-    // every MMA has completed (or none was issued), so no stage is being
-    // read or loaded: the first two Q tiles stage the output rows
+    // After a complete walk every MMA has completed and every stage was
+    // consumed, so no stage is being read or loaded: the first two Q tiles
+    // stage the output rows.  A key tile without steps loaded nothing.  A CTA
+    // that gave up may still have copies in flight into the stages, so it
+    // stores its zeros straight to global memory instead.
     named_bar_sync(1, 32 * SM_WARPS);
     const int r0 = k0 + sp * 32;
     const int nvalid = min(32, p.Skv - r0);
     uint8_t* stage = s.Q[0] + (warp - SM_WARP0) * 2048;
+    const bool staged = __all_sync(0xffffffffu, have || (ok && N == 0));
 #pragma unroll 1
     for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
+      uint16_t* base = which ? dk : dv;
+      uint16_t* orow = base + ((size_t)bc * p.Skv + r0) * HEAD_DIM + 32 * g;
+      if (!staged) {
+        warp_zero_rows(orow, 32, nvalid);
+        continue;
+      }
       uint32_t pk[16];
       if (have) {
         const float sc = which ? p.scale : 1.f;
@@ -514,8 +550,6 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) pk[cc] = 0u;
       }
-      uint16_t* base = which ? dk : dv;
-      uint16_t* orow = base + ((size_t)bc * p.Skv + r0) * HEAD_DIM + 32 * g;
       warp_store_rows32(stage, pk, orow, nvalid);
     }
   }
@@ -536,10 +570,21 @@ cudaError_t launch_dkdv(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                                        (int)kv_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int nKT = (p.Skv + KV_TILE - 1) / KV_TILE;
-  dim3 grid((unsigned)(nKT * p.B * p.Hkv));
-  kern<<<grid, kv_side::NUM_THREADS, kv_side::SMEM_BYTES, st>>>(tQ, tdO, tK, tV, (uint16_t*)dk,
-                                                                 (uint16_t*)dv, p);
-  return cudaGetLastError();
+  // closed-form masks: programmatic stream serialization behind the
+  // preprocess kernel, so that this grid's set-up and K / V loads overlap its
+  // tail (block masks read the select tables as soon as a CTA starts, so the
+  // table kernels before them must have completed)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(nKT * p.B * p.Hkv));
+  cfg.blockDim = dim3(kv_side::NUM_THREADS);
+  cfg.dynamicSmemBytes = kv_side::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.mask_kind == MK_BLOCK ? 0 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, tQ, tdO, tK, tV, (uint16_t*)dk, (uint16_t*)dv, p);
 }
 
 }  // namespace mab

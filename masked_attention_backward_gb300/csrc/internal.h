@@ -61,6 +61,7 @@ struct AttnParams {
   int compensated;     // backward: P and dS enter the contractions as high part + remainder
   const int* seqlen_q; // [B] valid query rows per batch, or nullptr (= Sq)
   const int* seqlen_k; // [B] valid keys per batch, or nullptr (= Skv)
+  int num_sms;         // SMs of the device (CTAs resident at once in one-CTA-per-SM grids)
 };
 
 #ifdef __CUDACC__

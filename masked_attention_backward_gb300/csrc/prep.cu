@@ -36,6 +36,10 @@ k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
   const int h = bh % Hq, b = bh / Hq;
   const int row0 = blk * PREP_BLOCK_ROWS + warp * ROWS_PER_WARP;
   const size_t head_rows = (size_t)bh * Sq;
+  // the dK/dV kernel behind this one (launched with programmatic
+  // serialization) may be scheduled once every block of this grid has
+  // started; it waits for this grid's completion before it reads any result
+  grid_launch_dependents();
   // rows past the batch's length are outside the problem: treated like the
   // padding (Delta 0, -lse log2 e = -inf, no dSink term)
   const int Lq = seqlen_q ? min(max(seqlen_q[b], 0), Sq) : Sq;

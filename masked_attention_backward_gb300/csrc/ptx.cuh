@@ -90,6 +90,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
+// Bounded wait that ignores the CTA's abort flag, for the way out of a CTA
+// that gave up: its own copies and MMAs still in flight must land before it
+// frees TMEM or exits.  Returns false when the limit runs out.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity,
+                                           unsigned long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
 // Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -107,6 +120,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
+}
+
+// Brings one box of a tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
 }
 
 // 1-D bulk copy global -> shared; src, dst 16-byte aligned, bytes % 16 == 0.
@@ -312,6 +332,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                                unsigned int tag) {
   const bool ok = mbar_wait(bar, parity, w, tag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Warp-uniform form of mbar_drain.
+__device__ __forceinline__ bool mbar_drain_warp(uint32_t bar, uint32_t parity,
+                                                unsigned long long timeout_ns) {
+  const bool ok = mbar_drain(bar, parity, timeout_ns);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -204,6 +204,17 @@ struct KVCursor {
   }
 };
 
+// Step n of a KVWalk: query head hh of the group and query sub-tile r,
+// head-major with ascending sub-tiles (the cursor advances here).  Key tiles
+// t and t + 1 of a kv head, which run side by side, then read the same query
+// rows two steps apart, so the second read comes from L2.
+__device__ __forceinline__ void kv_step(const AttnParams& p, const KVWalk& w, KVCursor& cur,
+                                        int* hh, int* r) {
+  *hh = cur.hh;
+  *r = w.tile(p, cur.hh, cur.idx);
+  cur.next(p, w);
+}
+
 // Store 32 rows x 64 columns (16-bit elements, packed as 32 u32 per lane, one
 // row per lane) through a per-warp 4 KB staging buffer so that global stores
 // are 128-byte coalesced.  out_row0 points at column col0 of the warp's first
@@ -247,6 +258,17 @@ __device__ __forceinline__ void warp_store_rows32(uint8_t* stage, const uint32_t
     if (row < nvalid) *reinterpret_cast<uint4*>(out_row0 + (size_t)row * HEAD_DIM + c * 8) = v;
   }
   __syncwarp();
+}
+
+// Zeros for `ncols` 16-bit columns (a multiple of 8) of 32 rows, one row per
+// lane, stored straight to global memory (rows >= nvalid skipped).  Used by
+// a CTA that gave up waiting, whose shared-memory staging space may still be
+// the target of a copy in flight.
+__device__ __forceinline__ void warp_zero_rows(uint16_t* out_row0, int ncols, int nvalid) {
+  const int lane = threadIdx.x & 31;
+  if (lane >= nvalid) return;
+  uint4* dst = reinterpret_cast<uint4*>(out_row0 + (size_t)lane * HEAD_DIM);
+  for (int c = 0; c < ncols / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 }  // namespace mab

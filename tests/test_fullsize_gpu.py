@@ -13,8 +13,10 @@ the benchmark times (one attn_bwd call over the whole problem).
   forward at this size would take minutes), compared against the oracle in
   exact mode (its own fp64 statistics): dq on sampled rows of every head; dk,
   dv on sampled key rows and dsink of the first kv-head group, whose 8 query
-  heads get a complete oracle forward; plus the column-sum property of dv on
-  every kv head, which holds at any size.
+  heads get a complete oracle forward; in parity mode (the CUDA forward's O
+  and LSE fed to the oracle as they are to the backward) dk, dv on sampled key
+  rows of kv heads 3 and 7 and dsink of all 64 heads; plus the column-sum
+  property of dv on every kv head, which holds at any size.
 """
 import numpy as np
 import pytest
@@ -106,6 +108,19 @@ def test_fullsize_causal_16k_sampled(cuda_lib, compensated):
     compare("dv", dv.reshape(-1, D)[cols], ref_dv, wl.dtype)
     ref_ds = oracle.dsink(pb, lse_full, dl)[:g]
     compare("dsink", dsink[:g], ref_ds, wl.dtype, min_frac=1.0)
+
+    # parity mode on the device's own statistics (the backward takes O and LSE
+    # as given, like every other parity case): dK, dV on sampled key rows of
+    # kv heads 3 and 7 (groups other than the first, reached by key tiles far
+    # into the grid) and dSink of every head
+    o64 = oracle._f64(o_gpu.cpu())
+    lse64 = lse_gpu.double().cpu().numpy()
+    dl_g = oracle.delta(pb, o64, dO64)
+    cols_g = np.concatenate([c * S + rng.choice(S, size=128, replace=False) for c in (3, 7)])
+    rk, rv = oracle.dkdv_cols(pb, q64, k64, v64, dO64, lse64, dl_g, cols_g.astype(np.int64))
+    compare("dk (kv heads 3, 7)", dk.reshape(-1, D)[cols_g], rk, wl.dtype)
+    compare("dv (kv heads 3, 7)", dv.reshape(-1, D)[cols_g], rv, wl.dtype)
+    compare("dsink (all heads)", dsink, oracle.dsink(pb, lse64, dl_g), wl.dtype, min_frac=1.0)
 
     # any size: sum_j dV_j = sum_{h in group} sum_i (1 - exp(sink_h - lse_i)) dO_i, per kv head
     w = 1.0 - torch.exp(sink.double().view(1, -1, 1) - lse_gpu.double())
