@@ -53,42 +53,61 @@ class _Problem(ctypes.Structure):
     ]
 
 
+def compile_source(src: str, out: str) -> str:
+    """Compile a C source of the oracle's interface into a shared library."""
+    tmp = out + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", src, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c into _build/liboracle.so (OpenMP if available)."""
     os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    base = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
-    try:
-        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
-                       capture_output=True)
-    except subprocess.CalledProcessError:
-        subprocess.run(base, check=True, capture_output=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+    return compile_source(_SRC, _LIB_PATH)
+
+
+def _bind(lib):
+    """Declare the argument types of every entry point of a loaded build."""
+    vp, i64 = ctypes.c_void_p, ctypes.c_int64
+    pp = ctypes.POINTER(_Problem)
+    lib.om_forward_rows.argtypes = [pp, vp, vp, vp, i64, vp, vp, vp]
+    lib.om_delta.argtypes = [pp, vp, vp, vp]
+    lib.om_dq_rows.argtypes = [pp, vp, vp, vp, vp, vp, vp, i64, vp, vp]
+    lib.om_dkdv_cols.argtypes = [pp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp]
+    lib.om_dsink.argtypes = [pp, vp, vp, vp]
+    lib.om_mask_transpose.argtypes = [i64, i64, i64, vp, vp]
+    lib.om_select_tables.argtypes = [i64, i64, i64, i64, i64, vp,
+                                     i64, i64, vp, vp, i64, i64, vp, vp]
+    lib.om_count_visible.argtypes = [pp]
+    lib.om_count_visible.restype = ctypes.c_int64
+    lib.om_num_threads.restype = ctypes.c_int
+    return lib
+
+
+def use_library(path: str) -> None:
+    """Route every later call of this process to another build of oracle.c.
+
+    Used by the mutation test, which compiles altered copies of the source in
+    a child process and checks that each one fails at least one pin."""
+    global _lib
+    with _lock:
+        _lib = _bind(ctypes.CDLL(path))
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            vp, i64 = ctypes.c_void_p, ctypes.c_int64
-            pp = ctypes.POINTER(_Problem)
-            lib.om_forward_rows.argtypes = [pp, vp, vp, vp, i64, vp, vp, vp]
-            lib.om_delta.argtypes = [pp, vp, vp, vp]
-            lib.om_dq_rows.argtypes = [pp, vp, vp, vp, vp, vp, vp, i64, vp, vp]
-            lib.om_dkdv_cols.argtypes = [pp, vp, vp, vp, vp, vp, vp, i64, vp, vp, vp]
-            lib.om_dsink.argtypes = [pp, vp, vp, vp]
-            lib.om_mask_transpose.argtypes = [i64, i64, i64, vp, vp]
-            lib.om_select_tables.argtypes = [i64, i64, i64, i64, i64, vp,
-                                             i64, i64, vp, vp, i64, i64, vp, vp]
-            lib.om_count_visible.argtypes = [pp]
-            lib.om_count_visible.restype = ctypes.c_int64
-            lib.om_num_threads.restype = ctypes.c_int
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
 
 

@@ -29,6 +29,8 @@ def _brute(mask, Sq, Skv, bx, by, tq, tk):
     (5000 // 8, 7000 // 8, 48, 80, 128, 64),
     (97, 97, 128, 128, 64, 64),
     (300, 260, 7, 13, 32, 16),
+    # blocks that start on the last row / key of a tile (63 = 64 - 1, 127 = 128 - 1)
+    (300, 400, 63, 127, 64, 128),
 ])
 def test_select_tables_brute_force(Sq, Skv, bx, by, tq, tk):
     rng = np.random.default_rng(Sq + Skv)
