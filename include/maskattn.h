@@ -106,14 +106,31 @@ typedef enum { ATTN_FLAG_COMPENSATED = 1 } attn_flag_t;
  * q, O, dO and LSE hold there, and such a key has dK = dV = 0 whatever finite
  * values k and v hold there.  This is the variable-length
  * batch on the padded BHSD layout: each sequence starts at row 0 of its batch
- * element.  4-byte aligned. */
+ * element.  4-byte aligned.
+ *
+ * Packed variable lengths: cu_seqlens_q and cu_seqlens_k, when not NULL (both,
+ * with seqlen_q and seqlen_k NULL), are device int32 arrays [B + 1] of
+ * cumulative sequence offsets: sequence b owns tokens [cu_seqlens_q[b],
+ * cu_seqlens_q[b + 1]) of q, o, dO and dq, which are then token-major
+ * [total_q, Hq, 128] tensors, and tokens [cu_seqlens_k[b], cu_seqlens_k[b + 1])
+ * of k, v, dk and dv, [total_k, Hkv, 128]; lse is float32 [Hq, total_q].
+ * total_q and total_k (>= 1) are the token counts of those tensors, known to
+ * the caller; Sq and Skv of the shape are the longest sequence lengths (they
+ * size the workspace and the block mask, whose rows and columns count from
+ * each sequence's start, as the causal and sliding-window rules do).  Offsets
+ * are clamped to [0, total] and lengths to [0, Sq] / [0, Skv]; every write
+ * stays inside the sequence's own tokens, and tokens no sequence owns are not
+ * written.  4-byte aligned. */
 typedef struct {
   int kind; /* attn_mask_kind_t */
   int window;
   int bx, by;
   const uint8_t* block_mask;
-  const int* seqlen_q; /* device [B] or NULL */
-  const int* seqlen_k; /* device [B] or NULL */
+  const int* seqlen_q;     /* device [B] or NULL */
+  const int* seqlen_k;     /* device [B] or NULL */
+  const int* cu_seqlens_q; /* device [B + 1] or NULL: packed layout */
+  const int* cu_seqlens_k; /* device [B + 1] or NULL */
+  int total_q, total_k;    /* packed layout: tokens in the query / key tensors */
 } attn_mask_desc_t;
 
 /* Workspace bytes needed by attn_fwd and attn_bwd for this shape and mask.

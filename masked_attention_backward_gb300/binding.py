@@ -38,7 +38,9 @@ ATTN_FLAG_COMPENSATED = 1
 class attn_mask_desc_t(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("window", ctypes.c_int), ("bx", ctypes.c_int),
                 ("by", ctypes.c_int), ("block_mask", ctypes.c_void_p),
-                ("seqlen_q", ctypes.c_void_p), ("seqlen_k", ctypes.c_void_p)]
+                ("seqlen_q", ctypes.c_void_p), ("seqlen_k", ctypes.c_void_p),
+                ("cu_seqlens_q", ctypes.c_void_p), ("cu_seqlens_k", ctypes.c_void_p),
+                ("total_q", ctypes.c_int), ("total_k", ctypes.c_int)]
 
 
 class AttnError(RuntimeError):
@@ -152,15 +154,29 @@ class Mask:
     block_mask: Optional[torch.Tensor] = None   # uint8 [B,Hq,nQB,nKB] on the device
     seqlen_q: Optional[torch.Tensor] = None     # int32 [B] on the device: valid query rows
     seqlen_k: Optional[torch.Tensor] = None     # int32 [B] on the device: valid keys
+    # packed layout: int32 [B + 1] cumulative offsets on the device, the
+    # longest lengths (the shape's Sq, Skv) and the tensors' token counts
+    cu_seqlens_q: Optional[torch.Tensor] = None
+    cu_seqlens_k: Optional[torch.Tensor] = None
+    max_seqlen_q: int = 0
+    max_seqlen_k: int = 0
+    total_q: int = 0
+    total_k: int = 0
+
+    @property
+    def packed(self) -> bool:
+        return self.cu_seqlens_q is not None
 
     def desc(self) -> attn_mask_desc_t:
         def ptr(t):
             return t.data_ptr() if t is not None else None
-        for t, n in ((self.seqlen_q, "seqlen_q"), (self.seqlen_k, "seqlen_k")):
+        for t, n in ((self.seqlen_q, "seqlen_q"), (self.seqlen_k, "seqlen_k"),
+                     (self.cu_seqlens_q, "cu_seqlens_q"), (self.cu_seqlens_k, "cu_seqlens_k")):
             if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
                 raise ValueError(f"{n} must be a contiguous int32 tensor")
         return attn_mask_desc_t(self.kind, self.window, self.bx, self.by, ptr(self.block_mask),
-                                ptr(self.seqlen_q), ptr(self.seqlen_k))
+                                ptr(self.seqlen_q), ptr(self.seqlen_k), ptr(self.cu_seqlens_q),
+                                ptr(self.cu_seqlens_k), self.total_q, self.total_k)
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -171,10 +187,32 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
-def shape_of(q: torch.Tensor, k: torch.Tensor, flags: int = 0) -> attn_shape_t:
+def shape_of(q: torch.Tensor, k: torch.Tensor, flags: int = 0,
+             mask: Optional[Mask] = None) -> attn_shape_t:
+    """BHSD tensors [B,H,S,D]; or, with a packed mask, token-major [T,H,D]
+    tensors whose batch and longest lengths come from the mask."""
+    if mask is not None and mask.packed:
+        _, Hq, D = q.shape
+        _, Hkv, _ = k.shape
+        B = mask.cu_seqlens_q.numel() - 1
+        return attn_shape_t(B, Hq, Hkv, mask.max_seqlen_q, mask.max_seqlen_k, D, _dtype_code(q),
+                            flags)
     B, Hq, Sq, D = q.shape
     _, Hkv, Skv, _ = k.shape
     return attn_shape_t(B, Hq, Hkv, Sq, Skv, D, _dtype_code(q), flags)
+
+
+def packed_mask(kind: int, seqlens_q, seqlens_k, device, window: int = 0, bx: int = 1,
+                by: int = 1, block_mask: Optional[torch.Tensor] = None) -> Mask:
+    """Mask for the packed layout from per-sequence lengths (host integers)."""
+    import itertools
+    lq, lk = [int(x) for x in seqlens_q], [int(x) for x in seqlens_k]
+    cq = [0] + list(itertools.accumulate(lq))
+    ck = [0] + list(itertools.accumulate(lk))
+    return Mask(kind=kind, window=window, bx=bx, by=by, block_mask=block_mask,
+                cu_seqlens_q=torch.tensor(cq, dtype=torch.int32, device=device),
+                cu_seqlens_k=torch.tensor(ck, dtype=torch.int32, device=device),
+                max_seqlen_q=max(lq), max_seqlen_k=max(lk), total_q=cq[-1], total_k=ck[-1])
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -203,9 +241,10 @@ def fwd(q, k, v, sink, mask: Mask, scale: float, ws: Optional[torch.Tensor] = No
     """Forward; returns (o, lse)."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, n)
-    shape = shape_of(q, k)
+    shape = shape_of(q, k, mask=mask)
     o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    lse_shape = (q.shape[1], q.shape[0]) if mask.packed else q.shape[:3]   # [Hq, T] when packed
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
     if ws is None:
         ws = workspace(shape, mask, q.device)
     r = attn_fwd(shape, _ptr(q), _ptr(k), _ptr(v), _ptr(sink), mask.desc(), scale, _ptr(o),
@@ -221,7 +260,7 @@ def bwd(q, k, v, o, dO, lse, sink, mask: Mask, scale: float, ws: Optional[torch.
     compensated: P and dS enter the contractions as high part + remainder."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (lse, "lse")):
         _check(t, n)
-    shape = shape_of(q, k, ATTN_FLAG_COMPENSATED if compensated else 0)
+    shape = shape_of(q, k, ATTN_FLAG_COMPENSATED if compensated else 0, mask=mask)
     if out is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         dsink = torch.empty_like(sink) if sink is not None else None

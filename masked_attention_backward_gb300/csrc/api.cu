@@ -60,6 +60,14 @@ attn_status_t check_shape_mask(const attn_shape_t* sh, const attn_mask_desc_t* m
   }
   if ((mk->seqlen_q && !aligned(mk->seqlen_q, 4)) || (mk->seqlen_k && !aligned(mk->seqlen_k, 4)))
     return ATTN_ERR_INVALID_ARG;
+  // packed layout: both offset arrays, no per-batch length arrays, and the
+  // token totals of the tensors (which bound every access)
+  if (mk->cu_seqlens_q || mk->cu_seqlens_k) {
+    if (!mk->cu_seqlens_q || !mk->cu_seqlens_k || mk->seqlen_q || mk->seqlen_k ||
+        !aligned(mk->cu_seqlens_q, 4) || !aligned(mk->cu_seqlens_k, 4) || mk->total_q < 1 ||
+        mk->total_k < 1)
+      return ATTN_ERR_INVALID_ARG;
+  }
   if (sh->D != HEAD_DIM) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
@@ -170,6 +178,12 @@ AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const W
   p.compensated = (sh->flags & ATTN_FLAG_COMPENSATED) ? 1 : 0;
   p.seqlen_q = mk->seqlen_q;
   p.seqlen_k = mk->seqlen_k;
+  if (mk->cu_seqlens_q) {
+    p.cu_q = mk->cu_seqlens_q;
+    p.cu_k = mk->cu_seqlens_k;
+    p.total_q = mk->total_q;
+    p.total_k = mk->total_k;
+  }
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) == cudaSuccess &&
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
@@ -178,6 +192,17 @@ AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const W
 }
 
 attn_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// Tensor map of a query-side (H = Hq, S = Sq) or key-side (H = Hkv, S = Skv)
+// tensor: BHSD [B*H, S, 128], or token-major [total, H, 128] in the packed
+// layout; boxes of `rows` rows of one head either way.
+bool make_map(CUtensorMap* m, const void* base, bool bf16, const attn_shape_t* sh,
+              const attn_mask_desc_t* mk, bool query_side, uint32_t rows) {
+  const int H = query_side ? sh->Hq : sh->Hkv;
+  if (mk->cu_seqlens_q)
+    return make_thd_map(m, base, bf16, query_side ? mk->total_q : mk->total_k, H, rows);
+  return make_bhsd_map(m, base, bf16, (int64_t)sh->B * H, query_side ? sh->Sq : sh->Skv, rows);
+}
 
 // ---- optional per-kernel events (attn_profile_enable) ----
 // The mutex is taken only by calls made while profiling is on (and by the
@@ -279,11 +304,10 @@ attn_status_t attn_fwd(const attn_shape_t* shape, const void* q, const void* k, 
   AttnParams p = params_of(shape, mask, L, w, scale);
   p.sink = sink;
   p.lse_out = lse;
-  const int BH = shape->B * shape->Hq, BHkv = shape->B * shape->Hkv;
   CUtensorMap tQ, tK, tV;
-  if (!make_bhsd_map(&tQ, q, bf16, BH, shape->Sq, Q_TILE) ||
-      !make_bhsd_map(&tK, k, bf16, BHkv, shape->Skv, Q_SUB) ||
-      !make_bhsd_map(&tV, v, bf16, BHkv, shape->Skv, Q_SUB))
+  if (!make_map(&tQ, q, bf16, shape, mask, true, Q_TILE) ||
+      !make_map(&tK, k, bf16, shape, mask, false, Q_SUB) ||
+      !make_map(&tV, v, bf16, shape, mask, false, Q_SUB))
     return ATTN_ERR_CUDA;
   std::unique_lock<std::mutex> lock(g_prof.mu, std::defer_lock);
   const bool prof = prof_lock(lock);
@@ -319,19 +343,18 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
   const bool bf16 = shape->dtype == ATTN_BF16;
   AttnParams p = params_of(shape, mask, L, w, scale);
   const Dims d = dims_of(shape, mask);
-  const int BH = shape->B * shape->Hq, BHkv = shape->B * shape->Hkv;
 
   // dK/dV walk query sub-tiles of KV_SUB rows over key tiles of KV_TILE rows;
   // dQ walks key sub-tiles of Q_SUB rows over query tiles of Q_TILE rows.
   CUtensorMap tQs, tdOs, tKt, tVt, tQt, tdOt, tKs, tVs;
-  if (!make_bhsd_map(&tQs, q, bf16, BH, shape->Sq, KV_SUB) ||
-      !make_bhsd_map(&tdOs, dO, bf16, BH, shape->Sq, KV_SUB) ||
-      !make_bhsd_map(&tKt, k, bf16, BHkv, shape->Skv, KV_TILE) ||
-      !make_bhsd_map(&tVt, v, bf16, BHkv, shape->Skv, KV_TILE) ||
-      !make_bhsd_map(&tQt, q, bf16, BH, shape->Sq, Q_TILE) ||
-      !make_bhsd_map(&tdOt, dO, bf16, BH, shape->Sq, Q_TILE) ||
-      !make_bhsd_map(&tKs, k, bf16, BHkv, shape->Skv, Q_SUB) ||
-      !make_bhsd_map(&tVs, v, bf16, BHkv, shape->Skv, Q_SUB))
+  if (!make_map(&tQs, q, bf16, shape, mask, true, KV_SUB) ||
+      !make_map(&tdOs, dO, bf16, shape, mask, true, KV_SUB) ||
+      !make_map(&tKt, k, bf16, shape, mask, false, KV_TILE) ||
+      !make_map(&tVt, v, bf16, shape, mask, false, KV_TILE) ||
+      !make_map(&tQt, q, bf16, shape, mask, true, Q_TILE) ||
+      !make_map(&tdOt, dO, bf16, shape, mask, true, Q_TILE) ||
+      !make_map(&tKs, k, bf16, shape, mask, false, Q_SUB) ||
+      !make_map(&tVs, v, bf16, shape, mask, false, Q_SUB))
     return ATTN_ERR_CUDA;
 
   std::unique_lock<std::mutex> lock(g_prof.mu, std::defer_lock);
@@ -342,7 +365,8 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
     e = launch_preprocess(bf16, o, dO, lse, sink, reinterpret_cast<float*>(w + L.nlse2),
                           reinterpret_cast<float*>(w + L.delta),
                           reinterpret_cast<float*>(w + L.dsink_part), shape->B, shape->Hq,
-                          shape->Sq, d.Sq_pad, mask->seqlen_q, st);
+                          shape->Sq, d.Sq_pad, mask->seqlen_q, mask->cu_seqlens_q,
+                          mask->total_q, st);
   }
   if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) {
     ProfScope ps(prof, "k_mask_tables", st);

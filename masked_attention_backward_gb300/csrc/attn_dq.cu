@@ -218,11 +218,12 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
           // Q / dO tiles are not loaded
           mbar_arrive(qbar);
         } else {
+          const RowAddr qa = row_q(p, un.bh / p.Hq, un.h, un.q0);
           mbar_arrive_expect_tx(qbar, 4 * Q_TILE * 128);
-          tma_load_3d(smem_u32(s.Q), &tQ, 0, un.q0, un.bh, qbar);
-          tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, un.q0, un.bh, qbar);
-          tma_load_3d(smem_u32(s.dO), &tdO, 0, un.q0, un.bh, qbar);
-          tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, un.q0, un.bh, qbar);
+          tma_load_3d(smem_u32(s.Q), &tQ, 0, qa.c1, qa.c2, qbar);
+          tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, qa.c1, qa.c2, qbar);
+          tma_load_3d(smem_u32(s.dO), &tdO, 0, qa.c1, qa.c2, qbar);
+          tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, qa.c1, qa.c2, qbar);
           q_loaded = j;
         }
         for (int n = 0; n < un.walk.cnt; ++n, ++m, rg.next()) {
@@ -260,11 +261,12 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
             s.step_vis[st] = w;
           }
           const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
+          const RowAddr ka = row_k(p, un.kvh / p.Hkv, un.kvh % p.Hkv, t * Q_SUB);
           mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
-          tma_load_3d(smem_u32(s.K[st]), &tK, 0, t * Q_SUB, un.kvh, fb);
-          tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, t * Q_SUB, un.kvh, fb);
-          tma_load_3d(smem_u32(s.V[st]), &tV, 0, t * Q_SUB, un.kvh, fb);
-          tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, t * Q_SUB, un.kvh, fb);
+          tma_load_3d(smem_u32(s.K[st]), &tK, 0, ka.c1, ka.c2, fb);
+          tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, ka.c1, ka.c2, fb);
+          tma_load_3d(smem_u32(s.V[st]), &tV, 0, ka.c1, ka.c2, fb);
+          tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, ka.c1, ka.c2, fb);
         }
       }
       if (!ok) {
@@ -380,11 +382,14 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       const bool have = acc_ok && un.walk.cnt > 0;
       tc_fence_after();
       const int r0 = un.q0 + sp * 32;
-      uint16_t* orow = dq + ((size_t)un.bh * p.Sq + r0) * HEAD_DIM + 64 * g;
+      const int bq = un.bh / p.Hq;
+      const RowAddr oa = row_q(p, bq, un.h, r0);
+      const int nvalid = rows_to_store_q(p, bq, r0);
+      uint16_t* orow = dq + oa.elem + 64 * g;
       if (!__all_sync(0xffffffffu, acc_ok)) {
         // the CTA gave up: a copy may still be landing in the Q tile, so the
         // zeros go straight to global memory
-        warp_zero_rows(orow, 64, min(32, p.Sq - r0));
+        warp_zero_rows(orow, 64, nvalid, oa.stride);
         return;
       }
       if (have) {
@@ -406,7 +411,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s.bar_acc_empty));
-      warp_store_rows(stage, pk, orow, min(32, p.Sq - r0));
+      warp_store_rows(stage, pk, orow, nvalid, oa.stride);
       // the next TMA load into the Q tile (after unit_free) comes after this
       // warp's generic accesses to it
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -546,7 +551,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
 
 cudaError_t launch_dq(bool bf16, const AttnParams& p, const CUtensorMap& tQ, const CUtensorMap& tdO,
                       const CUtensorMap& tK, const CUtensorMap& tV, void* dq, cudaStream_t st) {
-  const bool varlen = p.seqlen_q != nullptr || p.seqlen_k != nullptr;
+  const bool varlen = p.seqlen_q != nullptr || p.seqlen_k != nullptr || p.cu_q != nullptr;
   using Kern = decltype(&k_dq<true, false, false>);
   static const Kern table[2][2][2] = {
       {{k_dq<false, false, false>, k_dq<false, false, true>},

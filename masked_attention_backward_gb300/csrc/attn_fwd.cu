@@ -218,9 +218,10 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
           // tile is not loaded
           mbar_arrive(qbar);
         } else {
+          const RowAddr qa = row_q(p, un.bh / p.Hq, un.h, un.q0);
           mbar_arrive_expect_tx(qbar, 2 * Q_TILE * 128);
-          tma_load_3d(smem_u32(s.Q), &tQ, 0, un.q0, un.bh, qbar);
-          tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, un.q0, un.bh, qbar);
+          tma_load_3d(smem_u32(s.Q), &tQ, 0, qa.c1, qa.c2, qbar);
+          tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, qa.c1, qa.c2, qbar);
           q_loaded = j;
         }
         for (int n = 0; n < un.walk.cnt; ++n, ++m, rg.next()) {
@@ -233,11 +234,12 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
           const int t = un.walk.tile(n);
           s.step_t[st] = t;  // published by the arrive below together with the loads
           const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
+          const RowAddr ka = row_k(p, un.kvh / p.Hkv, un.kvh % p.Hkv, t * Q_SUB);
           mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
-          tma_load_3d(smem_u32(s.K[st]), &tK, 0, t * Q_SUB, un.kvh, fb);
-          tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, t * Q_SUB, un.kvh, fb);
-          tma_load_3d(smem_u32(s.V[st]), &tV, 0, t * Q_SUB, un.kvh, fb);
-          tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, t * Q_SUB, un.kvh, fb);
+          tma_load_3d(smem_u32(s.K[st]), &tK, 0, ka.c1, ka.c2, fb);
+          tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, ka.c1, ka.c2, fb);
+          tma_load_3d(smem_u32(s.V[st]), &tV, 0, ka.c1, ka.c2, fb);
+          tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, ka.c1, ka.c2, fb);
         }
       }
       if (!ok) {
@@ -395,16 +397,25 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
         for (int c = 0; c < 16; ++c) pk[16 * half + c] = pack2<BF16>(acc[2 * c], acc[2 * c + 1]);
       }
       const int r0 = un.q0 + sp * 32;
+      const int bq = un.bh / p.Hq, h = un.bh % p.Hq;
+      const int nvalid = rows_to_store_q(p, bq, r0);
       if (r0 + lane >= un.Lq) lse = INFINITY;  // past the batch's length: outside the problem
-      if (grp == 0 && r0 + lane < p.Sq) p.lse_out[(size_t)un.bh * p.Sq + r0 + lane] = lse;
-      uint16_t* orow = out + ((size_t)un.bh * p.Sq + r0) * HEAD_DIM + 64 * grp;
+      if (grp == 0 && lane < nvalid) {
+        // lse: [B*Hq, Sq] in the BHSD layout, [Hq, total_q] in the packed one
+        const size_t li = p.cu_q ? (size_t)h * p.total_q + packed_off(p.cu_q, bq, p.total_q) + r0 +
+                                       lane
+                                 : (size_t)un.bh * p.Sq + r0 + lane;
+        p.lse_out[li] = lse;
+      }
+      const RowAddr oa = row_q(p, bq, h, r0);
+      uint16_t* orow = out + oa.elem + 64 * grp;
       if (!__all_sync(0xffffffffu, ok && (N == 0 || have))) {
         // the CTA gave up: a copy may still be landing in the Q tile, so the
         // zeros go straight to global memory
-        warp_zero_rows(orow, 64, min(32, p.Sq - r0));
+        warp_zero_rows(orow, 64, nvalid, oa.stride);
         return;
       }
-      warp_store_rows(stage, pk, orow, min(32, p.Sq - r0));
+      warp_store_rows(stage, pk, orow, nvalid, oa.stride);
       // the next TMA load into the Q tile comes after this warp's generic
       // accesses to it
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -168,11 +168,12 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       tma_prefetch_desc(&tK);
       tma_prefetch_desc(&tV);
       const uint32_t kvbar = smem_u32(&s.bar_kv_full);
+      const RowAddr ka = row_k(p, b, c, k0);
       mbar_arrive_expect_tx(kvbar, 4 * KV_TILE * 128);
-      tma_load_3d(smem_u32(s.K), &tK, 0, k0, bc, kvbar);
-      tma_load_3d(smem_u32(s.K + KV_TILE * 128), &tK, 64, k0, bc, kvbar);
-      tma_load_3d(smem_u32(s.V), &tV, 0, k0, bc, kvbar);
-      tma_load_3d(smem_u32(s.V + KV_TILE * 128), &tV, 64, k0, bc, kvbar);
+      tma_load_3d(smem_u32(s.K), &tK, 0, ka.c1, ka.c2, kvbar);
+      tma_load_3d(smem_u32(s.K + KV_TILE * 128), &tK, 64, ka.c1, ka.c2, kvbar);
+      tma_load_3d(smem_u32(s.V), &tV, 0, ka.c1, ka.c2, kvbar);
+      tma_load_3d(smem_u32(s.V + KV_TILE * 128), &tV, 64, ka.c1, ka.c2, kvbar);
     }
   }
   if (warp == 1) {
@@ -203,10 +204,11 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       const int succ = (int)blockIdx.x + p.num_sms;
       if (N <= 64 && succ < (int)gridDim.x) {
         const int t2 = succ / BHkv, bc2 = succ % BHkv;
-        tma_prefetch_l2_3d(&tK, 0, t2 * KV_TILE, bc2);
-        tma_prefetch_l2_3d(&tK, 64, t2 * KV_TILE, bc2);
-        tma_prefetch_l2_3d(&tV, 0, t2 * KV_TILE, bc2);
-        tma_prefetch_l2_3d(&tV, 64, t2 * KV_TILE, bc2);
+        const RowAddr a2 = row_k(p, bc2 / p.Hkv, bc2 % p.Hkv, t2 * KV_TILE);
+        tma_prefetch_l2_3d(&tK, 0, a2.c1, a2.c2);
+        tma_prefetch_l2_3d(&tK, 64, a2.c1, a2.c2);
+        tma_prefetch_l2_3d(&tV, 0, a2.c1, a2.c2);
+        tma_prefetch_l2_3d(&tV, 64, a2.c1, a2.c2);
       }
       KVCursor cur;
       cur.start(p, walk);
@@ -255,10 +257,11 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         mbar_arrive_expect_tx(fb, 4 * KV_SUB * 128 + 2 * KV_SUB * 4);
         uint8_t* sq = stage_q(s, st);
         uint8_t* sd = stage_do(s, st);
-        tma_load_3d(smem_u32(sq), &tQ, 0, r * KV_SUB, bh, fb);
-        tma_load_3d(smem_u32(sq + KV_SUB * 128), &tQ, 64, r * KV_SUB, bh, fb);
-        tma_load_3d(smem_u32(sd), &tdO, 0, r * KV_SUB, bh, fb);
-        tma_load_3d(smem_u32(sd + KV_SUB * 128), &tdO, 64, r * KV_SUB, bh, fb);
+        const RowAddr qa = row_q(p, b, c * p.group + hh, r * KV_SUB);
+        tma_load_3d(smem_u32(sq), &tQ, 0, qa.c1, qa.c2, fb);
+        tma_load_3d(smem_u32(sq + KV_SUB * 128), &tQ, 64, qa.c1, qa.c2, fb);
+        tma_load_3d(smem_u32(sd), &tdO, 0, qa.c1, qa.c2, fb);
+        tma_load_3d(smem_u32(sd + KV_SUB * 128), &tdO, 64, qa.c1, qa.c2, fb);
         const size_t srow = (size_t)bh * p.Sq_pad + (size_t)r * KV_SUB;
         bulk_load(smem_u32(s.nlse2[st]), p.nlse2 + srow, KV_SUB * 4, fb);
         bulk_load(smem_u32(s.delta[st]), p.delta + srow, KV_SUB * 4, fb);
@@ -527,15 +530,16 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     // stores its zeros straight to global memory instead.
     named_bar_sync(1, 32 * SM_WARPS);
     const int r0 = k0 + sp * 32;
-    const int nvalid = min(32, p.Skv - r0);
+    const int nvalid = rows_to_store_k(p, b, r0);
+    const RowAddr oa = row_k(p, b, c, r0);
     uint8_t* stage = s.Q[0] + (warp - SM_WARP0) * 2048;
     const bool staged = __all_sync(0xffffffffu, have || (ok && N == 0));
 #pragma unroll 1
     for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
       uint16_t* base = which ? dk : dv;
-      uint16_t* orow = base + ((size_t)bc * p.Skv + r0) * HEAD_DIM + 32 * g;
+      uint16_t* orow = base + oa.elem + 32 * g;
       if (!staged) {
-        warp_zero_rows(orow, 32, nvalid);
+        warp_zero_rows(orow, 32, nvalid, oa.stride);
         continue;
       }
       uint32_t pk[16];
@@ -550,7 +554,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
 #pragma unroll
         for (int cc = 0; cc < 16; ++cc) pk[cc] = 0u;
       }
-      warp_store_rows32(stage, pk, orow, nvalid);
+      warp_store_rows32(stage, pk, orow, nvalid, oa.stride);
     }
   }
   tc_fence_before();

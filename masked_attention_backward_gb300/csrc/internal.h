@@ -62,23 +62,78 @@ struct AttnParams {
   const int* seqlen_q; // [B] valid query rows per batch, or nullptr (= Sq)
   const int* seqlen_k; // [B] valid keys per batch, or nullptr (= Skv)
   int num_sms;         // SMs of the device (CTAs resident at once in one-CTA-per-SM grids)
+  // Packed layout: sequence b holds tokens [cu_q[b], cu_q[b + 1]) of the
+  // token-major tensors q, o, dO, dq [total_q, Hq, 128] (lse [Hq, total_q])
+  // and [cu_k[b], cu_k[b + 1]) of k, v, dk, dv [total_k, Hkv, 128]; Sq and
+  // Skv are then the longest lengths.  nullptr / 0 for the BHSD layout.
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;
 };
 
 #ifdef __CUDACC__
+// Token offset and valid length of sequence b in a packed tensor of `total`
+// tokens, the length clamped to [0, smax] and to the tensor's end.
+__device__ __forceinline__ int packed_off(const int* cu, int b, int total) {
+  return min(max(cu[b], 0), total);
+}
+__device__ __forceinline__ int packed_len(const int* cu, int b, int total, int smax) {
+  const int o = packed_off(cu, b, total);
+  return min(min(max(cu[b + 1], o), total) - o, smax);
+}
+
 // Valid query rows / keys of batch b: the per-batch lengths clamped to
 // [0, Sq] / [0, Skv], or the full lengths.
 __device__ __forceinline__ int len_q(const AttnParams& p, int b) {
+  if (p.cu_q) return packed_len(p.cu_q, b, p.total_q, p.Sq);
   return p.seqlen_q ? min(max(p.seqlen_q[b], 0), p.Sq) : p.Sq;
 }
 __device__ __forceinline__ int len_k(const AttnParams& p, int b) {
+  if (p.cu_k) return packed_len(p.cu_k, b, p.total_k, p.Skv);
   return p.seqlen_k ? min(max(p.seqlen_k[b], 0), p.Skv) : p.Skv;
+}
+
+// Where row `row` of head h (of H heads) of batch b lives.  BHSD [B*H, S, 128]
+// tensor maps take the coordinates (row, b*H + h); packed [T, H, 128] maps
+// take (h, token).  In memory a row starts at element `elem` and consecutive
+// rows of the head are `stride` elements apart.
+struct RowAddr {
+  int c1, c2;
+  size_t elem;
+  int stride;
+};
+__device__ __forceinline__ RowAddr row_q(const AttnParams& p, int b, int h, int row) {
+  if (p.cu_q) {
+    const int tok = packed_off(p.cu_q, b, p.total_q) + row;
+    return {h, tok, ((size_t)tok * p.Hq + h) * 128, p.Hq * 128};
+  }
+  const int bh = b * p.Hq + h;
+  return {row, bh, ((size_t)bh * p.Sq + row) * 128, 128};
+}
+__device__ __forceinline__ RowAddr row_k(const AttnParams& p, int b, int c, int row) {
+  if (p.cu_k) {
+    const int tok = packed_off(p.cu_k, b, p.total_k) + row;
+    return {c, tok, ((size_t)tok * p.Hkv + c) * 128, p.Hkv * 128};
+  }
+  const int bc = b * p.Hkv + c;
+  return {row, bc, ((size_t)bc * p.Skv + row) * 128, 128};
+}
+// Rows of head h (batch b) the epilogue writes starting at row r0, at most
+// 32: up to the padded length in the BHSD layout (rows past a batch's valid
+// length are zeros there), only the sequence's own rows in the packed one.
+__device__ __forceinline__ int rows_to_store_q(const AttnParams& p, int b, int r0) {
+  return max(0, min(32, (p.cu_q ? len_q(p, b) : p.Sq) - r0));
+}
+__device__ __forceinline__ int rows_to_store_k(const AttnParams& p, int b, int r0) {
+  return max(0, min(32, (p.cu_k ? len_k(p, b) : p.Skv) - r0));
 }
 #endif
 
 // ---- launchers (each returns the launch error, if any) ----
 cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const float* lse,
                               const float* sink, float* nlse2, float* delta, float* part, int B,
-                              int Hq, int Sq, int Sq_pad, const int* seqlen_q, cudaStream_t st);
+                              int Hq, int Sq, int Sq_pad, const int* seqlen_q, const int* cu_q,
+                              int total_q, cudaStream_t st);
 cudaError_t launch_dsink_finalize(const float* part, int Hq, int nparts, float* dsink,
                                   cudaStream_t st);
 cudaError_t launch_mask_transpose(const uint8_t* mask, uint8_t* maskT, int BH, int nqb, int nkb,

@@ -28,7 +28,8 @@ __global__ void __launch_bounds__(256, 4)
 k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
              const float* __restrict__ lse, const float* __restrict__ sink,
              float* __restrict__ nlse2, float* __restrict__ delta, float* __restrict__ part, int Hq,
-             int Sq, int Sq_pad, int nparts, const int* __restrict__ seqlen_q) {
+             int Sq, int Sq_pad, int nparts, const int* __restrict__ seqlen_q,
+             const int* __restrict__ cu_q, int total_q) {
   constexpr int ROWS_PER_WARP = PREP_BLOCK_ROWS / 8;  // 8
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, l16 = lane & 15;
@@ -42,14 +43,24 @@ k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
   grid_launch_dependents();
   // rows past the batch's length are outside the problem: treated like the
   // padding (Delta 0, -lse log2 e = -inf, no dSink term)
-  const int Lq = seqlen_q ? min(max(seqlen_q[b], 0), Sq) : Sq;
+  const int Lq = cu_q ? packed_len(cu_q, b, total_q, Sq)
+                      : (seqlen_q ? min(max(seqlen_q[b], 0), Sq) : Sq);
+  // BHSD: row r of (b, h) is row bh * Sq + r of O and dO, lse [B*Hq, Sq];
+  // packed: token cu_q[b] + r of the token-major O and dO, lse [Hq, total_q]
+  const int off = cu_q ? packed_off(cu_q, b, total_q) : 0;
+  auto row_elem16 = [&](int row) -> size_t {  // uint4 index of a row's first element
+    return cu_q ? ((size_t)(off + row) * Hq + h) * 16 : (head_rows + row) * 16;
+  };
+  auto lse_index = [&](int row) -> size_t {
+    return cu_q ? (size_t)h * total_q + off + row : head_rows + row;
+  };
 
   uint4 vo[ROWS_PER_WARP / 2], vd[ROWS_PER_WARP / 2];
 #pragma unroll
   for (int it = 0; it < ROWS_PER_WARP / 2; ++it) {
     int row = row0 + it * 2 + half;
     if (row < Lq) {
-      size_t idx = (head_rows + row) * 16 + l16;
+      size_t idx = row_elem16(row) + l16;
       vo[it] = __ldg(O + idx);
       vd[it] = __ldg(dO + idx);
     } else {
@@ -76,7 +87,7 @@ k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
     if (l16 == 0) {
       size_t o = (size_t)bh * Sq_pad + row;
       if (row < Lq) {
-        float l2 = lse[head_rows + row] * LOG2E;
+        float l2 = lse[lse_index(row)] * LOG2E;
         delta[o] = acc;
         nlse2[o] = -l2;
         if (sink) term_acc += exp2f(sink2 - l2) * acc;
@@ -190,15 +201,16 @@ __global__ void k_build_sel(AttnParams p, int* __restrict__ sel_k, int* __restri
 
 cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const float* lse,
                               const float* sink, float* nlse2, float* delta, float* part, int B,
-                              int Hq, int Sq, int Sq_pad, const int* seqlen_q, cudaStream_t st) {
+                              int Hq, int Sq, int Sq_pad, const int* seqlen_q, const int* cu_q,
+                              int total_q, cudaStream_t st) {
   dim3 grid(Sq_pad / PREP_BLOCK_ROWS, B * Hq);
   int nparts = B * (Sq_pad / PREP_BLOCK_ROWS);
   if (bf16)
     k_preprocess<true><<<grid, 256, 0, st>>>((const uint4*)O, (const uint4*)dO, lse, sink, nlse2,
-                                              delta, part, Hq, Sq, Sq_pad, nparts, seqlen_q);
+                                              delta, part, Hq, Sq, Sq_pad, nparts, seqlen_q, cu_q, total_q);
   else
     k_preprocess<false><<<grid, 256, 0, st>>>((const uint4*)O, (const uint4*)dO, lse, sink, nlse2,
-                                               delta, part, Hq, Sq, Sq_pad, nparts, seqlen_q);
+                                               delta, part, Hq, Sq, Sq_pad, nparts, seqlen_q, cu_q, total_q);
   return cudaGetLastError();
 }
 

@@ -218,9 +218,10 @@ __device__ __forceinline__ void kv_step(const AttnParams& p, const KVWalk& w, KV
 // Store 32 rows x 64 columns (16-bit elements, packed as 32 u32 per lane, one
 // row per lane) through a per-warp 4 KB staging buffer so that global stores
 // are 128-byte coalesced.  out_row0 points at column col0 of the warp's first
-// row; row stride is HEAD_DIM elements; rows >= nvalid are skipped.
+// row; rows are `stride` elements apart; rows >= nvalid are skipped.
 __device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint32_t (&pk)[32],
-                                                uint16_t* out_row0, int nvalid) {
+                                                uint16_t* out_row0, int nvalid,
+                                                int stride = HEAD_DIM) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
@@ -232,7 +233,7 @@ __device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint32_t (
   for (int k = 0; k < 8; ++k) {
     int row = k * 4 + (lane >> 3), c = lane & 7;
     uint4 v = *reinterpret_cast<const uint4*>(stage + row * 128 + ((c ^ (row & 7)) << 4));
-    if (row < nvalid) *reinterpret_cast<uint4*>(out_row0 + (size_t)row * HEAD_DIM + c * 8) = v;
+    if (row < nvalid) *reinterpret_cast<uint4*>(out_row0 + (size_t)row * stride + c * 8) = v;
   }
   __syncwarp();
 }
@@ -240,10 +241,11 @@ __device__ __forceinline__ void warp_store_rows(uint8_t* stage, const uint32_t (
 // Store 32 rows x 32 columns (16-bit elements, packed as 16 u32 per lane, one
 // row per lane) through a per-warp 2 KB staging buffer, so that each global
 // store instruction writes 8 rows of 64 contiguous bytes.  out_row0 points at
-// column col0 of the warp's first row; row stride is HEAD_DIM elements; rows
+// column col0 of the warp's first row; rows are `stride` elements apart; rows
 // >= nvalid are skipped.
 __device__ __forceinline__ void warp_store_rows32(uint8_t* stage, const uint32_t (&pk)[16],
-                                                  uint16_t* out_row0, int nvalid) {
+                                                  uint16_t* out_row0, int nvalid,
+                                                  int stride = HEAD_DIM) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -255,7 +257,7 @@ __device__ __forceinline__ void warp_store_rows32(uint8_t* stage, const uint32_t
   for (int k = 0; k < 4; ++k) {
     int row = k * 8 + (lane >> 2), c = lane & 3;
     uint4 v = *reinterpret_cast<const uint4*>(stage + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
-    if (row < nvalid) *reinterpret_cast<uint4*>(out_row0 + (size_t)row * HEAD_DIM + c * 8) = v;
+    if (row < nvalid) *reinterpret_cast<uint4*>(out_row0 + (size_t)row * stride + c * 8) = v;
   }
   __syncwarp();
 }
@@ -264,10 +266,11 @@ __device__ __forceinline__ void warp_store_rows32(uint8_t* stage, const uint32_t
 // lane, stored straight to global memory (rows >= nvalid skipped).  Used by
 // a CTA that gave up waiting, whose shared-memory staging space may still be
 // the target of a copy in flight.
-__device__ __forceinline__ void warp_zero_rows(uint16_t* out_row0, int ncols, int nvalid) {
+__device__ __forceinline__ void warp_zero_rows(uint16_t* out_row0, int ncols, int nvalid,
+                                               int stride = HEAD_DIM) {
   const int lane = threadIdx.x & 31;
   if (lane >= nvalid) return;
-  uint4* dst = reinterpret_cast<uint4*>(out_row0 + (size_t)lane * HEAD_DIM);
+  uint4* dst = reinterpret_cast<uint4*>(out_row0 + (size_t)lane * stride);
   for (int c = 0; c < ncols / 8; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
 }
 

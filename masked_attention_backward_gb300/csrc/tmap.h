@@ -48,4 +48,23 @@ inline bool make_bhsd_map(CUtensorMap* m, const void* base, bool bf16, int64_t B
   return r == CUDA_SUCCESS;
 }
 
+// Token-major [T, H, 128] tensor (the packed variable-length layout) as a
+// 3-D tensor map (head dim, head, token) with a box of 64 x 1 x rows: one box
+// is `rows` consecutive tokens of one head, laid out in shared memory exactly
+// like a box of the BHSD map.  Tokens past T read as zero.
+inline bool make_thd_map(CUtensorMap* m, const void* base, bool bf16, int64_t T, int64_t H,
+                         uint32_t rows_box) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
+  cuuint32_t box[3] = {64, 1, rows_box};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace mab

@@ -57,6 +57,22 @@ def test_status_strings(lib):
     # per-batch length arrays must be 4-byte aligned
     (_shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None, 4098, None), mab.ATTN_ERR_INVALID_ARG),
     (_shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None, None, 4097), mab.ATTN_ERR_INVALID_ARG),
+    # packed layout: both offset arrays, aligned, no per-batch lengths beside
+    # them, and token totals of at least one
+    (_shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None, None, None, 4096, 8192, 100, 90),
+     mab.ATTN_OK),
+    (_shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None, None, None, 4096, None, 100, 90),
+     mab.ATTN_ERR_INVALID_ARG),
+    (_shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None, None, None, None, 8192, 100, 90),
+     mab.ATTN_ERR_INVALID_ARG),
+    (_shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None, 4096, None, 4096, 8192, 100, 90),
+     mab.ATTN_ERR_INVALID_ARG),
+    (_shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None, None, None, 4098, 8192, 100, 90),
+     mab.ATTN_ERR_INVALID_ARG),
+    (_shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None, None, None, 4096, 8192, 0, 90),
+     mab.ATTN_ERR_INVALID_ARG),
+    (_shape(), mab.attn_mask_desc_t(0, 0, 1, 1, None, None, None, 4096, 8192, 100, -1),
+     mab.ATTN_ERR_INVALID_ARG),
 ])
 def test_workspace_size_validation(lib, shape, mask, want):
     r, _ = mab.attn_workspace_size(shape, mask)
