@@ -163,12 +163,30 @@ class ClockSampler:
                 "samples": len(rows), "reasons": sorted(reasons)}
 
 
-def gpu_inputs(wl, device):
+def _pack(x, lens):
+    """[B, H, S, D] -> token-major [sum(lens), H, D] (sequence b's first lens[b] rows)"""
+    return torch.cat([x[b, :, :L].transpose(0, 1) for b, L in enumerate(lens)], dim=0).contiguous()
+
+
+def gpu_inputs(wl, device, packed=False):
+    """Device inputs of a workload; O and LSE from the CUDA forward.  packed:
+    a variable-length workload in the packed layout (token-major tensors and
+    cumulative sequence offsets) instead of the padded BHSD one."""
     from masked_attention_backward_gb300 import binding as mab
     inp = make_inputs(wl)
-    q, k, v, dO = (t.to(device) for t in (inp.q, inp.k, inp.v, inp.dO))
     sink = inp.sink.to(device) if inp.sink is not None else None
     bm = inp.block_mask.to(device) if inp.block_mask is not None else None
+    if packed:
+        lq = [int(x) for x in inp.seqlen_q]
+        lk = [int(x) for x in inp.seqlen_k]
+        q, dO = (_pack(t, lq).to(device) for t in (inp.q, inp.dO))
+        k, v = (_pack(t, lk).to(device) for t in (inp.k, inp.v))
+        mask = mab.packed_mask(wl.mask_kind, lq, lk, device, window=wl.window, bx=wl.bx,
+                               by=wl.by, block_mask=bm)
+        o, lse = mab.fwd(q, k, v, sink, mask, wl.scale)
+        torch.cuda.synchronize()
+        return inp, dict(q=q, k=k, v=v, o=o, dO=dO, lse=lse, sink=sink, mask=mask)
+    q, k, v, dO = (t.to(device) for t in (inp.q, inp.k, inp.v, inp.dO))
     lq = inp.seqlen_q.to(device) if inp.seqlen_q is not None else None
     lk = inp.seqlen_k.to(device) if inp.seqlen_k is not None else None
     mask = mab.Mask(kind=wl.mask_kind, window=wl.window, bx=wl.bx, by=wl.by, block_mask=bm,
@@ -307,7 +325,8 @@ def run_ours(args, rank, world, local):
         elif n == "k_dq":
             d["tflops"] = round(fl["dq"] / (a * 1e-3) / 1e12, 1)
         elif n == "k_preprocess":
-            d["gbps"] = round(measure.algorithmic_bytes(wl)["preprocess"] / (a * 1e-3) / 1e9, 1)
+            d["gbps"] = round(measure.algorithmic_bytes(wl, 0, inp.seqlen_q, inp.seqlen_k)
+                              ["preprocess"] / (a * 1e-3) / 1e9, 1)
         kernels[n] = d
 
     # ---- the forward that produced O and LSE, timed on its own (not part of
@@ -382,7 +401,9 @@ TABLE_WORKLOADS = [
     ("blocksparse_random30_s8192", "tensor"),
     ("blocksparse_bigbird_5000x7000", "hbm"),
     ("gqa_sink_varlen_causal_b8_s2048", "tensor"),
+    ("gqa_sink_varlen_causal_b8_s2048_packed", "tensor"),
 ]
+PACKED_SUFFIX = "_packed"
 
 
 def time_workload(name, bound, device, peaks, min_steps=20, min_seconds=0.6, max_steps=2000):
@@ -391,13 +412,15 @@ def time_workload(name, bound, device, peaks, min_steps=20, min_seconds=0.6, max
     passed, with nvidia-smi sampling the clocks; then up to 20 steps with the
     library's per-kernel events on."""
     from masked_attention_backward_gb300 import binding as mab
-    wl = BY_NAME[name]
-    inp, t = gpu_inputs(wl, device)
+    packed = name.endswith(PACKED_SUFFIX)
+    wl = BY_NAME[name[:-len(PACKED_SUFFIX)] if packed else name]
+    inp, t = gpu_inputs(wl, device, packed=packed)
     pairs = measure.visible_pairs(wl, inp.block_mask, inp.seqlen_q, inp.seqlen_k)
     fl = measure.flops(wl, pairs)
     ab = measure.algorithmic_bytes(
-        wl, 0 if inp.block_mask is None else int(inp.block_mask.numel()))
-    ws = mab.workspace(mab.shape_of(t["q"], t["k"]), t["mask"], device)
+        wl, 0 if inp.block_mask is None else int(inp.block_mask.numel()), inp.seqlen_q,
+        inp.seqlen_k)
+    ws = mab.workspace(mab.shape_of(t["q"], t["k"], mask=t["mask"]), t["mask"], device)
     out = (torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"]),
            torch.empty_like(t["sink"]) if t["sink"] is not None else None)
     stream = torch.cuda.current_stream()
@@ -445,7 +468,11 @@ def time_workload(name, bound, device, peaks, min_steps=20, min_seconds=0.6, max
            "tflops": round(tflops, 1), "frac_tensor_end_to_end": round(tflops / tpk, 4),
            "alg_bytes": int(ab["total"]), "gbps_alg": round(gbps, 1),
            "frac_hbm": round(gbps / peaks["hbm_gbs"], 4), "bound": bound,
-           "dtype": wl.dtype, "config": workload_config(wl, pairs, fl, inp), "clocks": clk}
+           "dtype": wl.dtype, "config": dict(workload_config(wl, pairs, fl, inp),
+                                             **({"layout": "packed (token-major tensors, "
+                                                           "cumulative sequence offsets)"}
+                                                if packed else {})),
+           "clocks": clk}
     kd = {}
     for kname, v in kern.items():
         a = float(np.mean(v))

@@ -62,13 +62,19 @@ def flops(wl: Workload, pairs: int) -> dict:
             "fwd": 4 * D * pairs}
 
 
-def algorithmic_bytes(wl: Workload, block_mask_bytes: int = 0) -> dict:
+def algorithmic_bytes(wl: Workload, block_mask_bytes: int = 0, seqlen_q=None,
+                      seqlen_k=None) -> dict:
     """Bytes each tensor must cross HBM once: q, k, v, o, dO, lse read; dq, dk,
-    dv written (plus sink / dsink and the block mask)."""
+    dv written (plus sink / dsink and the block mask).  With per-batch lengths
+    only the rows and keys inside them count."""
     e = 2
-    q = wl.B * wl.Hq * wl.Sq * wl.D * e
-    kv = wl.B * wl.Hkv * wl.Skv * wl.D * e
-    lse = wl.B * wl.Hq * wl.Sq * 4
+    rows_q = wl.B * wl.Sq if seqlen_q is None else int(sum(min(max(int(x), 0), wl.Sq)
+                                                           for x in seqlen_q))
+    rows_k = wl.B * wl.Skv if seqlen_k is None else int(sum(min(max(int(x), 0), wl.Skv)
+                                                            for x in seqlen_k))
+    q = wl.Hq * rows_q * wl.D * e
+    kv = wl.Hkv * rows_k * wl.D * e
+    lse = wl.Hq * rows_q * 4
     read = 3 * q + 2 * kv + lse + block_mask_bytes
     write = q + 2 * kv
     return {"read": read, "write": write, "total": read + write,
