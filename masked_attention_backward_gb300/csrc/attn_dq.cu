@@ -218,7 +218,10 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
           // Q / dO tiles are not loaded
           mbar_arrive(qbar);
         } else {
-          const RowAddr qa = row_q(p, un.bh / p.Hq, un.h, un.q0);
+          // packed layout (always with per-batch lengths): token coordinates;
+          // BHSD: (row, head)
+          const RowAddr qa = VARLEN ? row_q(p, un.bh / p.Hq, un.h, un.q0)
+                                    : RowAddr{un.q0, un.bh, 0, HEAD_DIM};
           mbar_arrive_expect_tx(qbar, 4 * Q_TILE * 128);
           tma_load_3d(smem_u32(s.Q), &tQ, 0, qa.c1, qa.c2, qbar);
           tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, qa.c1, qa.c2, qbar);
@@ -261,7 +264,8 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
             s.step_vis[st] = w;
           }
           const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
-          const RowAddr ka = row_k(p, un.kvh / p.Hkv, un.kvh % p.Hkv, t * Q_SUB);
+          const RowAddr ka = VARLEN ? row_k(p, un.kvh / p.Hkv, un.kvh % p.Hkv, t * Q_SUB)
+                                    : RowAddr{t * Q_SUB, un.kvh, 0, HEAD_DIM};
           mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
           tma_load_3d(smem_u32(s.K[st]), &tK, 0, ka.c1, ka.c2, fb);
           tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, ka.c1, ka.c2, fb);
@@ -383,8 +387,10 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       tc_fence_after();
       const int r0 = un.q0 + sp * 32;
       const int bq = un.bh / p.Hq;
-      const RowAddr oa = row_q(p, bq, un.h, r0);
-      const int nvalid = rows_to_store_q(p, bq, r0);
+      const RowAddr oa =
+          VARLEN ? row_q(p, bq, un.h, r0)
+                 : RowAddr{r0, un.bh, ((size_t)un.bh * p.Sq + r0) * HEAD_DIM, HEAD_DIM};
+      const int nvalid = VARLEN ? rows_to_store_q(p, bq, r0) : min(32, p.Sq - r0);
       uint16_t* orow = dq + oa.elem + 64 * g;
       if (!__all_sync(0xffffffffu, acc_ok)) {
         // the CTA gave up: a copy may still be landing in the Q tile, so the

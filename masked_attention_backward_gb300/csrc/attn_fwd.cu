@@ -140,7 +140,9 @@ struct FwdDone {
 
 }  // namespace fwd_side
 
-template <bool BF16>
+// PACKED: the token-major layout with cumulative sequence offsets (the BHSD
+// instance keeps its plain row addressing).
+template <bool BF16, bool PACKED>
 __global__ void __launch_bounds__(fwd_side::NUM_THREADS, 1)
 k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tK,
            const __grid_constant__ CUtensorMap tV, uint16_t* __restrict__ out,
@@ -218,7 +220,8 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
           // tile is not loaded
           mbar_arrive(qbar);
         } else {
-          const RowAddr qa = row_q(p, un.bh / p.Hq, un.h, un.q0);
+          const RowAddr qa =
+              PACKED ? row_q(p, un.bh / p.Hq, un.h, un.q0) : RowAddr{un.q0, un.bh, 0, HEAD_DIM};
           mbar_arrive_expect_tx(qbar, 2 * Q_TILE * 128);
           tma_load_3d(smem_u32(s.Q), &tQ, 0, qa.c1, qa.c2, qbar);
           tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, qa.c1, qa.c2, qbar);
@@ -234,7 +237,8 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
           const int t = un.walk.tile(n);
           s.step_t[st] = t;  // published by the arrive below together with the loads
           const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
-          const RowAddr ka = row_k(p, un.kvh / p.Hkv, un.kvh % p.Hkv, t * Q_SUB);
+          const RowAddr ka = PACKED ? row_k(p, un.kvh / p.Hkv, un.kvh % p.Hkv, t * Q_SUB)
+                                    : RowAddr{t * Q_SUB, un.kvh, 0, HEAD_DIM};
           mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
           tma_load_3d(smem_u32(s.K[st]), &tK, 0, ka.c1, ka.c2, fb);
           tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, ka.c1, ka.c2, fb);
@@ -398,16 +402,18 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
       }
       const int r0 = un.q0 + sp * 32;
       const int bq = un.bh / p.Hq, h = un.bh % p.Hq;
-      const int nvalid = rows_to_store_q(p, bq, r0);
+      const int nvalid = PACKED ? rows_to_store_q(p, bq, r0) : min(32, p.Sq - r0);
       if (r0 + lane >= un.Lq) lse = INFINITY;  // past the batch's length: outside the problem
       if (grp == 0 && lane < nvalid) {
         // lse: [B*Hq, Sq] in the BHSD layout, [Hq, total_q] in the packed one
-        const size_t li = p.cu_q ? (size_t)h * p.total_q + packed_off(p.cu_q, bq, p.total_q) + r0 +
+        const size_t li = PACKED ? (size_t)h * p.total_q + packed_off(p.cu_q, bq, p.total_q) + r0 +
                                        lane
                                  : (size_t)un.bh * p.Sq + r0 + lane;
         p.lse_out[li] = lse;
       }
-      const RowAddr oa = row_q(p, bq, h, r0);
+      const RowAddr oa =
+          PACKED ? row_q(p, bq, h, r0)
+                 : RowAddr{r0, un.bh, ((size_t)un.bh * p.Sq + r0) * HEAD_DIM, HEAD_DIM};
       uint16_t* orow = out + oa.elem + 64 * grp;
       if (!__all_sync(0xffffffffu, ok && (N == 0 || have))) {
         // the CTA gave up: a copy may still be landing in the Q tile, so the
@@ -586,7 +592,9 @@ k_attn_fwd(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUten
 
 cudaError_t launch_fwd(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                        const CUtensorMap& tK, const CUtensorMap& tV, void* o, cudaStream_t st) {
-  auto kern = bf16 ? k_attn_fwd<true> : k_attn_fwd<false>;
+  const bool packed = p.cu_q != nullptr;
+  auto kern = bf16 ? (packed ? k_attn_fwd<true, true> : k_attn_fwd<true, false>)
+                   : (packed ? k_attn_fwd<false, true> : k_attn_fwd<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)fwd_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;

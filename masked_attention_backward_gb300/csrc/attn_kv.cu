@@ -1,12 +1,12 @@
 // attn_kv.cu -- key-stationary dK/dV kernel on tcgen05 / TMEM, fed by TMA.
 //
 // One CTA per (b, kv head c, KV_TILE key rows).  K and V of the tile are
-// loaded once; K is copied into TMEM.  The CTA walks every query head of the
+// loaded once into shared memory.  The CTA walks every query head of the
 // GQA group and, for each, every active query sub-tile r of KV_SUB rows
 // (closed-form range for causal / sliding / none, the key-major select table
 // for block masks):
-//   S^T  = K Q_r^T            (A = K from TMEM)
-//   dP^T = V dO_r^T           (A = V from shared memory)
+//   S^T  = K Q_r^T            (A = K, B = Q_r from shared memory)
+//   dP^T = V dO_r^T           (A = V, B = dO_r from shared memory)
 //   P^T  = exp2(S^T * scale*log2e - lse_r log2e),  dS^T = P^T (dP^T - Delta_r)
 //   dV  += P^T dO_r,  dK += dS^T Q_r          (A = P^T / dS^T from TMEM)
 // The group reduction happens in the TMEM accumulators; the epilogue scales
@@ -23,16 +23,17 @@
 // row layout the A operand of dV += P^T dO and dK += dS^T Q needs, so P^T and
 // dS^T go back into TMEM and never touch shared memory.
 //
-// TMEM columns (512): dV [0,128), dK [128,256), K as 16-bit pairs [256,320),
-// S^T [320,384), dP^T [384,448), packed P^T [448,480), packed dS^T
-// [480,512).  Softmax group g owns query columns 16 g .. 16 g + 15 of a
-// sub-tile, so the 16 queries of MMA K-step g sit at column 8 g of the packed
-// regions.  Because P^T and dS^T have regions of their own, the fp32 S^T and
-// dP^T buffers are free as soon as the softmax warps have loaded them into
-// registers: S^T(n+1) runs while the softmax warps turn S^T(n) into P^T(n),
-// and dP^T(n+1) while they turn dP^T(n) into dS^T(n).  Only the packed
-// regions wait for the accumulations: P^T(n+1) is written once dV(n) has
-// read P^T(n), dS^T(n+1) once dK(n) has read dS^T(n).
+// TMEM columns (512): dV [0,128), dK [128,256) and two step buffers of 128
+// columns at 256 and 384, step n using buffer n & 1: fp32 S^T in its first 64
+// columns, fp32 dP^T in the next 64.  Softmax group g owns query columns
+// 16 g .. 16 g + 15 of each half and writes its 16 packed P^T values over the
+// first 8 of its own S^T columns (and dS^T over its dP^T columns), so the 16
+// queries of MMA K-step g sit at column 16 g of the half.  S^T(n + 2) may
+// overwrite a buffer once dV(n) has read the P^T in it, dP^T(n + 2) once dK(n)
+// has read the dS^T: every MMA has a whole step in which to run ahead of the
+// softmax warps, and the softmax warps never wait for an MMA to finish
+// reading, only for their own inputs.  K stays in shared memory: S^T = K Q^T
+// reads both operands from there, as dP^T = V dO^T does.
 //
 // Four warps issue MMAs into the one tensor pipe, each waiting only on its own
 // inputs: warp 1 S^T(m), warp 2 dP^T(m), warp 3 dV(n), warp 4 dK(n).  The pipe
@@ -52,42 +53,33 @@ namespace mab {
 
 namespace kv_side {
 
-constexpr int STAGES = 5;      // Q/dO ring depth; the last stage reuses K's tile
+constexpr int STAGES = 4;      // Q/dO ring depth
 constexpr int COL_DV = 0;
 constexpr int COL_DK = 128;
-constexpr int COL_KA = 256;    // K as the A operand (64 columns of 16-bit pairs)
-constexpr int COL_PLO = 256;   // compensated mode: P^T remainders (K stays in shared memory)
-constexpr int COL_DSLO = 288;  // compensated mode: dS^T remainders
-constexpr int COL_ST = 320;    // S^T, fp32
-constexpr int COL_DPT = 384;   // dP^T, fp32
-constexpr int COL_PT = 448;    // P^T, 16-bit pairs
-constexpr int COL_DST = 480;   // dS^T, 16-bit pairs
+constexpr int COL_BUF = 256;   // buffer b at COL_BUF + 128 b: S^T at +0, dP^T at +64
 constexpr int SM_WARPS = 16;   // softmax warps
 constexpr int SM_WARP0 = 5;     // first softmax warp
 constexpr int NUM_THREADS = 32 * (SM_WARP0 + SM_WARPS);
 
 struct __align__(1024) Smem {
-  uint8_t K[2 * KV_TILE * 128];  // dead once copied into TMEM: Q/dO stage 4
+  uint8_t K[2 * KV_TILE * 128];
   uint8_t V[2 * KV_TILE * 128];
-  uint8_t Q[STAGES - 1][2 * KV_SUB * 128];
-  uint8_t dO[STAGES - 1][2 * KV_SUB * 128];
+  uint8_t Q[STAGES][2 * KV_SUB * 128];   // the first two stages stage the epilogue rows
+  uint8_t dO[STAGES][2 * KV_SUB * 128];
   float nlse2[STAGES][KV_SUB];  // -lse log2(e) of the stage's query rows
   float delta[STAGES][KV_SUB];
   int step_r[STAGES];            // query sub-tile of the step in the stage
   int step_hh[STAGES];           // its query head within the group
   uint32_t step_vis[STAGES];     // aligned block masks: bit 4 sp + g = region (sp, g) visible
   uint64_t bar_kv_full;          // K, V landed
-  uint64_t bar_ka_full;          // K copied into TMEM (all softmax warps)
   uint64_t bar_q_full[STAGES];
   uint64_t bar_q_empty[STAGES];  // dV and dK of the step complete (one commit each)
-  uint64_t bar_s_full;           // S^T complete
-  uint64_t bar_s_free;           // S^T loaded by every softmax warp
-  uint64_t bar_dp_full;          // dP^T complete
-  uint64_t bar_dp_free;          // dP^T loaded by every softmax warp
-  uint64_t bar_p_full;           // P^T written by every softmax warp
-  uint64_t bar_pt_free;          // dV that read P^T complete
-  uint64_t bar_ds_full;          // dS^T written by every softmax warp
-  uint64_t bar_dst_free;         // dK that read dS^T complete
+  uint64_t bar_s_full[2];        // S^T of the buffer complete
+  uint64_t bar_dp_full[2];       // dP^T of the buffer complete
+  uint64_t bar_p_full[2];        // P^T written over the buffer's S^T (every softmax warp)
+  uint64_t bar_ds_full[2];       // dS^T written over the buffer's dP^T (every softmax warp)
+  uint64_t bar_s_free[2];        // dV that read the buffer's P^T complete
+  uint64_t bar_dp_free[2];       // dK that read the buffer's dS^T complete
   uint64_t bar_x_done[2];        // every S^T (0) / dP^T (1) MMA complete
   uint64_t bar_acc_full;         // every dV and dK MMA complete (one commit each)
   uint32_t tmem_base;
@@ -96,33 +88,25 @@ struct __align__(1024) Smem {
 
 constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
 static_assert(SMEM_BYTES <= 232448, "over the 227 KB of shared memory a CTA may use");
-static_assert(2 * KV_TILE * 128 == 2 * (2 * KV_SUB * 128), "stage 4 must fit in K's tile");
+static_assert(2 * (2 * KV_SUB * 128) >= SM_WARPS * 2048, "epilogue staging fits in two Q stages");
 
-// Q / dO tile of stage st (stage STAGES - 1 lives in K's tile once K is in TMEM).
-__device__ __forceinline__ uint8_t* stage_q(Smem& s, int st) {
-  return st < STAGES - 1 ? s.Q[st] : s.K;
-}
-__device__ __forceinline__ uint8_t* stage_do(Smem& s, int st) {
-  return st < STAGES - 1 ? s.dO[st] : s.K + 2 * KV_SUB * 128;
-}
-
-enum { TAG_KV = 0x201, TAG_KA, TAG_Q_EMPTY, TAG_Q_FULL, TAG_S_FREE, TAG_P_FULL, TAG_S_FULL,
-       TAG_DP_FULL, TAG_DS_FULL, TAG_ACC, TAG_X_DONE, TAG_DP_FREE, TAG_PT_FREE, TAG_DST_FREE };
+enum { TAG_KV = 0x201, TAG_Q_EMPTY = 0x203, TAG_Q_FULL, TAG_S_FREE, TAG_P_FULL, TAG_S_FULL,
+       TAG_DP_FULL, TAG_DS_FULL, TAG_ACC, TAG_X_DONE, TAG_DP_FREE };
 
 }  // namespace kv_side
 
-// HILO: P^T and dS^T enter dV and dK as a 16-bit high part (the packed
-// regions) plus a 16-bit remainder, packed the same way into the 64 columns
-// that otherwise hold K: K stays in shared memory (S^T is then issued with
-// both operands there, as dP^T is), so its tile is not a Q/dO stage and the
-// ring has one stage fewer.
-template <bool BF16, bool HILO>
+// HILO: P^T and dS^T enter dV and dK as a 16-bit high part plus a 16-bit
+// remainder, the remainder packed over the second 8 of the softmax group's
+// own columns.
+// PACKED: the token-major layout with cumulative sequence offsets (the BHSD
+// instances keep their plain row addressing).
+template <bool BF16, bool HILO, bool PACKED>
 __global__ void __launch_bounds__(kv_side::NUM_THREADS, 1)
 k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tdO,
        const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
        uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, const AttnParams p) {
   using namespace kv_side;
-  constexpr int NST = HILO ? STAGES - 1 : STAGES;  // Q/dO ring length
+  constexpr int NST = STAGES;  // Q/dO ring length
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -144,21 +128,19 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
   if (threadIdx.x == 0) {
     s.abort_flag = 0;
     mbar_init(smem_u32(&s.bar_kv_full), 1);
-    mbar_init(smem_u32(&s.bar_ka_full), SM_WARPS);
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(smem_u32(&s.bar_q_full[i]), 1);
       mbar_init(smem_u32(&s.bar_q_empty[i]), 2);
     }
-    mbar_init(smem_u32(&s.bar_s_full), 1);
-    mbar_init(smem_u32(&s.bar_s_free), SM_WARPS);
-    mbar_init(smem_u32(&s.bar_dp_full), 1);
-    mbar_init(smem_u32(&s.bar_dp_free), SM_WARPS);
-    mbar_init(smem_u32(&s.bar_p_full), SM_WARPS);
-    mbar_init(smem_u32(&s.bar_pt_free), 1);
-    mbar_init(smem_u32(&s.bar_ds_full), SM_WARPS);
-    mbar_init(smem_u32(&s.bar_dst_free), 1);
-    mbar_init(smem_u32(&s.bar_x_done[0]), 1);
-    mbar_init(smem_u32(&s.bar_x_done[1]), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.bar_s_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_dp_full[i]), 1);
+      mbar_init(smem_u32(&s.bar_p_full[i]), SM_WARPS);
+      mbar_init(smem_u32(&s.bar_ds_full[i]), SM_WARPS);
+      mbar_init(smem_u32(&s.bar_s_free[i]), 1);
+      mbar_init(smem_u32(&s.bar_dp_free[i]), 1);
+      mbar_init(smem_u32(&s.bar_x_done[i]), 1);
+    }
     mbar_init(smem_u32(&s.bar_acc_full), 2);
     fence_mbar_init();
     // K and V of the tile, loaded while the rest of the CTA sets up (they do
@@ -168,7 +150,7 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       tma_prefetch_desc(&tK);
       tma_prefetch_desc(&tV);
       const uint32_t kvbar = smem_u32(&s.bar_kv_full);
-      const RowAddr ka = row_k(p, b, c, k0);
+      const RowAddr ka = PACKED ? row_k(p, b, c, k0) : RowAddr{k0, bc, 0, HEAD_DIM};
       mbar_arrive_expect_tx(kvbar, 4 * KV_TILE * 128);
       tma_load_3d(smem_u32(s.K), &tK, 0, ka.c1, ka.c2, kvbar);
       tma_load_3d(smem_u32(s.K + KV_TILE * 128), &tK, 64, ka.c1, ka.c2, kvbar);
@@ -204,7 +186,8 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       const int succ = (int)blockIdx.x + p.num_sms;
       if (N <= 64 && succ < (int)gridDim.x) {
         const int t2 = succ / BHkv, bc2 = succ % BHkv;
-        const RowAddr a2 = row_k(p, bc2 / p.Hkv, bc2 % p.Hkv, t2 * KV_TILE);
+        const RowAddr a2 = PACKED ? row_k(p, bc2 / p.Hkv, bc2 % p.Hkv, t2 * KV_TILE)
+                                  : RowAddr{t2 * KV_TILE, bc2, 0, HEAD_DIM};
         tma_prefetch_l2_3d(&tK, 0, a2.c1, a2.c2);
         tma_prefetch_l2_3d(&tK, 64, a2.c1, a2.c2);
         tma_prefetch_l2_3d(&tV, 0, a2.c1, a2.c2);
@@ -237,10 +220,6 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         if (n >= NST &&
             !mbar_wait(smem_u32(&s.bar_q_empty[st]), ((n / NST) - 1) & 1, wc, TAG_Q_EMPTY))
           break;
-        // the last stage overwrites K's tile: wait until every softmax warp
-        // has copied K into TMEM
-        if (!HILO && n == STAGES - 1 && !mbar_wait(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA))
-          break;
         // the step's coordinates for the softmax warps, published by the
         // arrive below together with the loads
         s.step_r[st] = r;
@@ -255,9 +234,10 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         }
         const uint32_t fb = smem_u32(&s.bar_q_full[st]);
         mbar_arrive_expect_tx(fb, 4 * KV_SUB * 128 + 2 * KV_SUB * 4);
-        uint8_t* sq = stage_q(s, st);
-        uint8_t* sd = stage_do(s, st);
-        const RowAddr qa = row_q(p, b, c * p.group + hh, r * KV_SUB);
+        uint8_t* sq = s.Q[st];
+        uint8_t* sd = s.dO[st];
+        const RowAddr qa = PACKED ? row_q(p, b, c * p.group + hh, r * KV_SUB)
+                                  : RowAddr{r * KV_SUB, bh, 0, HEAD_DIM};
         tma_load_3d(smem_u32(sq), &tQ, 0, qa.c1, qa.c2, fb);
         tma_load_3d(smem_u32(sq + KV_SUB * 128), &tQ, 64, qa.c1, qa.c2, fb);
         tma_load_3d(smem_u32(sd), &tdO, 0, qa.c1, qa.c2, fb);
@@ -279,50 +259,28 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     constexpr uint32_t ID_S = idesc_f16(BF16, KV_TILE, KV_SUB, false, false);
     constexpr uint32_t ID_ACC = idesc_f16(BF16, KV_TILE, HEAD_DIM, false, true);
     if (warp == 1 || warp == 2) {
-      // warp 1: S^T(m) = K Q^T (A = K from TMEM, B = Q tile, K-major);
-      // warp 2: dP^T(m) = V dO^T (A = V tile, B = dO tile, both K-major in
-      // shared memory).  Each waits for the softmax warps to have loaded its
-      // previous result.
+      // warp 1: S^T(m) = K Q^T; warp 2: dP^T(m) = V dO^T, into buffer m & 1
+      // (A = K / V tile, B = Q / dO tile, both K-major in shared memory).
+      // Each waits for the accumulation that read the buffer two steps ago.
       const bool is_s = warp == 1;
-      const uint32_t free_bar = smem_u32(is_s ? &s.bar_s_free : &s.bar_dp_free);
-      const uint32_t full_bar = smem_u32(is_s ? &s.bar_s_full : &s.bar_dp_full);
-      const uint64_t aV = sdesc_sw128(smem_u32(s.V), 16, 1024);
-      const uint64_t aK = sdesc_sw128(smem_u32(s.K), 16, 1024);
-      bool ok = N == 0 || (is_s && !HILO ? mbar_wait_warp(smem_u32(&s.bar_ka_full), 0, wc, TAG_KA)
-                                         : mbar_wait_warp(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV));
+      const uint64_t aKV = sdesc_sw128(smem_u32(is_s ? s.K : s.V), 16, 1024);
+      bool ok = N == 0 || mbar_wait_warp(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV);
       for (int m = 0; ok && m < N; ++m) {
-        const int st = m % NST;
+        const int st = m % NST, bf = m & 1;
         ok = mbar_wait_warp(smem_u32(&s.bar_q_full[st]), (m / NST) & 1, wc, TAG_Q_FULL);
-        if (ok && m >= 1)
-          ok = mbar_wait_warp(free_bar, (m - 1) & 1, wc, is_s ? TAG_S_FREE : TAG_DP_FREE);
+        if (ok && m >= 2)
+          ok = mbar_wait_warp(smem_u32(is_s ? &s.bar_s_free[bf] : &s.bar_dp_free[bf]),
+                              ((m - 2) >> 1) & 1, wc, is_s ? TAG_S_FREE : TAG_DP_FREE);
         if (!ok) break;
         tc_fence_after();
-        if (is_s) {
-          const uint64_t bQ = sdesc_sw128(smem_u32(stage_q(s, st)), 16, 1024);
-          if constexpr (HILO) {
+        const uint64_t bB = sdesc_sw128(smem_u32(is_s ? s.Q[st] : s.dO[st]), 16, 1024);
+        const uint32_t d = tbase + COL_BUF + 128 * bf + (is_s ? 0 : 64);
 #pragma unroll
-            for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-              mma_ss_w(tbase + COL_ST,
-                       aK + (uint64_t)(((kk >> 2) * (KV_TILE * 128) + (kk & 3) * 32) >> 4),
-                       bQ + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                       kk > 0 ? 1u : 0u);
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-              mma_ts_w(tbase + COL_ST, tbase + COL_KA + 8 * kk,
-                       bQ + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                       kk > 0 ? 1u : 0u);
-          }
-        } else {
-          const uint64_t bO = sdesc_sw128(smem_u32(stage_do(s, st)), 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
-            mma_ss_w(tbase + COL_DPT,
-                     aV + (uint64_t)(((kk >> 2) * (KV_TILE * 128) + (kk & 3) * 32) >> 4),
-                     bO + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
-                     kk > 0 ? 1u : 0u);
-        }
-        mma_commit_w(full_bar);
+        for (int kk = 0; kk < HEAD_DIM / 16; ++kk)
+          mma_ss_w(d, aKV + (uint64_t)(((kk >> 2) * (KV_TILE * 128) + (kk & 3) * 32) >> 4),
+                   bB + (uint64_t)(((kk >> 2) * (KV_SUB * 128) + (kk & 3) * 32) >> 4), ID_S,
+                   kk > 0 ? 1u : 0u);
+        mma_commit_w(smem_u32(is_s ? &s.bar_s_full[bf] : &s.bar_dp_full[bf]));
       }
       // this warp's MMAs must be complete before TMEM is freed (also when the
       // CTA gave up, hence a wait that ignores the abort flag)
@@ -330,39 +288,38 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       mma_commit_w(done);
       mbar_drain_warp(done, 0, wc.timeout_ns);
     } else {
-      // warp 3: dV += P^T(n) dO; warp 4: dK += dS^T(n) Q (A from the packed
-      // regions, B MN-major).  Both commit to q_empty and acc_full, which
-      // complete on the two commits.
+      // warp 3: dV += P^T(n) dO; warp 4: dK += dS^T(n) Q (A = the packed
+      // values in buffer n & 1, B MN-major).  Each commit frees its half of
+      // the buffer; both commit to q_empty and acc_full, which complete on
+      // the two commits.
       const bool dkside = warp == 4;
       const uint32_t acc = tbase + (dkside ? COL_DK : COL_DV);
-      const uint32_t a = tbase + (dkside ? COL_DST : COL_PT);
-      const uint32_t full_bar = smem_u32(dkside ? &s.bar_ds_full : &s.bar_p_full);
-      const uint32_t free_bar = smem_u32(dkside ? &s.bar_dst_free : &s.bar_pt_free);
       bool ok = true;
       for (int n = 0; ok && n < N; ++n) {
-        const int st = n % NST;
-        ok = mbar_wait_warp(full_bar, n & 1, wc, dkside ? TAG_DS_FULL : TAG_P_FULL);
+        const int st = n % NST, bf = n & 1;
+        ok = mbar_wait_warp(smem_u32(dkside ? &s.bar_ds_full[bf] : &s.bar_p_full[bf]),
+                            (n >> 1) & 1, wc, dkside ? TAG_DS_FULL : TAG_P_FULL);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t a = tbase + COL_BUF + 128 * bf + (dkside ? 64 : 0);
         const uint64_t bB =
-            sdesc_sw128(smem_u32(dkside ? stage_q(s, st) : stage_do(s, st)), KV_SUB * 128, 1024);
+            sdesc_sw128(smem_u32(dkside ? s.Q[st] : s.dO[st]), KV_SUB * 128, 1024);
 #pragma unroll
         for (int kk = 0; kk < KV_SUB / 16; ++kk)
-          mma_ts_w(acc, a + 8 * kk, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC,
+          mma_ts_w(acc, a + 16 * kk, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC,
                    (n > 0 || kk > 0) ? 1u : 0u);
         if (HILO) {
-          const uint32_t lo = tbase + (dkside ? COL_DSLO : COL_PLO);
 #pragma unroll
           for (int kk = 0; kk < KV_SUB / 16; ++kk)
-            mma_ts_w(acc, lo + 8 * kk, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC, 1u);
+            mma_ts_w(acc, a + 16 * kk + 8, bB + (uint64_t)((kk * 2048) >> 4), ID_ACC, 1u);
         }
-        mma_commit_w(free_bar);
+        mma_commit_w(smem_u32(dkside ? &s.bar_dp_free[bf] : &s.bar_s_free[bf]));
         // S^T(n) and dP^T(n) completed before the softmax warps could write
         // P^T(n) / dS^T(n), so the two commits also free the Q / dO stage
         mma_commit_w(smem_u32(&s.bar_q_empty[st]));
       }
-      // completes when every MMA of both warps has (also on the abort path,
-      // so that TMEM is idle before it is freed)
+      // completes when every MMA of both warps has (also when the CTA gave
+      // up, so that TMEM is idle before it is freed)
       mma_commit_w(smem_u32(&s.bar_acc_full));
       mbar_drain_warp(smem_u32(&s.bar_acc_full), 0, wc.timeout_ns);
     }
@@ -373,27 +330,6 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     const int j = k0 + rloc;
     const uint32_t lane_base = tbase + ((uint32_t)(sp * 32) << 16);
     bool ok = true;
-    if (N > 0) ok = mbar_wait(smem_u32(&s.bar_kv_full), 0, wc, TAG_KV);
-    if (!HILO && ok && N > 0) {
-      // K rows into TMEM as 16-bit pairs (element 2c in the low half of column
-      // c): this warp copies d columns 32 g .. 32 g + 31 of its rows.
-      const int u0 = (g & 1) * 4;
-      const uint8_t* src = s.K + (g >> 1) * (KV_TILE * 128) + rloc * 128;
-      uint32_t w[16];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + (((u0 + u) ^ (rloc & 7)) << 4));
-        w[4 * u] = v.x;
-        w[4 * u + 1] = v.y;
-        w[4 * u + 2] = v.z;
-        w[4 * u + 3] = v.w;
-      }
-      tmem_st16(lane_base + COL_KA + 16 * g, w);
-      tmem_wait_st();
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&s.bar_ka_full));
 
     // signal one barrier from this warp once its TMEM accesses are done
     auto warp_arrive = [&](uint64_t* bar) {
@@ -404,18 +340,19 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     int flo, fhi;  // query sub-tiles that are entirely visible
     full_range_kv(p.mask_kind, p.window, Lq, Lk, k0, &flo, &fhi);
     for (int n = 0; ok && n < N; ++n) {
-      const int st = n % NST;
+      const int st = n % NST, bf = n & 1;
+      const uint32_t colS = COL_BUF + 128 * bf + 16 * g;  // this warp's S^T / P^T columns
       // ---- P^T(n) = exp2(S^T(n) * scale*log2e - lse log2e)
       // s_full implies the stage's loads landed; waiting on q_full as well
       // makes the bulk-copied -lse log2e / Delta rows visible to this thread
-      if (!mbar_wait(smem_u32(&s.bar_s_full), n & 1, wc, TAG_S_FULL) ||
+      if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (n >> 1) & 1, wc, TAG_S_FULL) ||
           !mbar_wait(smem_u32(&s.bar_q_full[st]), (n / NST) & 1, wc, TAG_Q_FULL)) {
         ok = false;
         break;
       }
       tc_fence_after();
       float sv[16];
-      tmem_ld16(lane_base + COL_ST + 16 * g, sv);
+      tmem_ld16(lane_base + colS, sv);
       const int r = s.step_r[st];
       // warp-uniform: the whole 64 x 128 sub-tile is visible
       const bool full = r >= flo && r <= fhi;
@@ -441,7 +378,6 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         lv[4 * q + 3] = L.w;
       }
       tmem_wait_ld_regs(sv);
-      warp_arrive(&s.bar_s_free);  // S^T(n + 1) may overwrite the buffer
       // an invisible logit becomes -inf, so its P is 0 (and so is its dS)
       if (!full) {
 #pragma unroll
@@ -458,24 +394,19 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         pv[2 * q + 1] = fast_exp2(x.y);
         pk[q] = pack2<BF16>(pv[2 * q], pv[2 * q + 1]);
       }
-      uint32_t pl[HILO ? 8 : 1];  // remainders P - high part
-      if (HILO) {
+      // over this warp's own S^T columns, which it has just loaded
+      tmem_st8(lane_base + colS, pk);
+      if constexpr (HILO) {
+        uint32_t pl[8];  // remainders P - high part
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float2 h = unpack2<BF16>(pk[q]);
-          pl[HILO ? q : 0] = pack2<BF16>(pv[2 * q] - h.x, pv[2 * q + 1] - h.y);
+          pl[q] = pack2<BF16>(pv[2 * q] - h.x, pv[2 * q + 1] - h.y);
         }
+        tmem_st8(lane_base + colS + 8, pl);
       }
-      // dV(n - 1) must have read P^T(n - 1)
-      if (n >= 1 && !mbar_wait(smem_u32(&s.bar_pt_free), (n - 1) & 1, wc, TAG_PT_FREE)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      tmem_st8(lane_base + COL_PT + 8 * g, pk);
-      if constexpr (HILO) tmem_st8(lane_base + COL_PLO + 8 * g, pl);
       tmem_wait_st();
-      warp_arrive(&s.bar_p_full);
+      warp_arrive(&s.bar_p_full[bf]);
 
       // ---- dS^T(n) = P^T(n) (dP^T(n) - Delta)
       const float4* d4 = reinterpret_cast<const float4*>(&s.delta[st][16 * g]);
@@ -488,15 +419,14 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         dl[4 * q + 2] = D.z;
         dl[4 * q + 3] = D.w;
       }
-      if (!mbar_wait(smem_u32(&s.bar_dp_full), n & 1, wc, TAG_DP_FULL)) {
+      if (!mbar_wait(smem_u32(&s.bar_dp_full[bf]), (n >> 1) & 1, wc, TAG_DP_FULL)) {
         ok = false;
         break;
       }
       tc_fence_after();
       float dp[16];
-      tmem_ld16(lane_base + COL_DPT + 16 * g, dp);
+      tmem_ld16(lane_base + colS + 64, dp);
       tmem_wait_ld_regs(dp);
-      warp_arrive(&s.bar_dp_free);  // dP^T(n + 1) may overwrite the buffer
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float2 ds = fmul2(make_float2(pv[2 * q], pv[2 * q + 1]),
@@ -504,20 +434,22 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
                                       make_float2(dl[2 * q], dl[2 * q + 1])));
         pk[q] = pack2<BF16>(ds.x, ds.y);
         if (HILO) {
-          const float2 h = unpack2<BF16>(pk[q]);
-          pl[HILO ? q : 0] = pack2<BF16>(ds.x - h.x, ds.y - h.y);
+          dp[2 * q] = ds.x;
+          dp[2 * q + 1] = ds.y;
         }
       }
-      // dK(n - 1) must have read dS^T(n - 1)
-      if (n >= 1 && !mbar_wait(smem_u32(&s.bar_dst_free), (n - 1) & 1, wc, TAG_DST_FREE)) {
-        ok = false;
-        break;
+      tmem_st8(lane_base + colS + 64, pk);
+      if constexpr (HILO) {
+        uint32_t pl[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float2 h = unpack2<BF16>(pk[q]);
+          pl[q] = pack2<BF16>(dp[2 * q] - h.x, dp[2 * q + 1] - h.y);
+        }
+        tmem_st8(lane_base + colS + 64 + 8, pl);
       }
-      tc_fence_after();
-      tmem_st8(lane_base + COL_DST + 8 * g, pk);
-      if constexpr (HILO) tmem_st8(lane_base + COL_DSLO + 8 * g, pl);
       tmem_wait_st();
-      warp_arrive(&s.bar_ds_full);
+      warp_arrive(&s.bar_ds_full[bf]);
     }
     // ---------------------------------------------------------- epilogue
     bool have = ok && N > 0;
@@ -530,8 +462,9 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     // stores its zeros straight to global memory instead.
     named_bar_sync(1, 32 * SM_WARPS);
     const int r0 = k0 + sp * 32;
-    const int nvalid = rows_to_store_k(p, b, r0);
-    const RowAddr oa = row_k(p, b, c, r0);
+    const int nvalid = PACKED ? rows_to_store_k(p, b, r0) : min(32, p.Skv - r0);
+    const RowAddr oa = PACKED ? row_k(p, b, c, r0)
+                              : RowAddr{r0, bc, ((size_t)bc * p.Skv + r0) * HEAD_DIM, HEAD_DIM};
     uint8_t* stage = s.Q[0] + (warp - SM_WARP0) * 2048;
     const bool staged = __all_sync(0xffffffffu, have || (ok && N == 0));
 #pragma unroll 1
@@ -568,8 +501,13 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
 cudaError_t launch_dkdv(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                         const CUtensorMap& tdO, const CUtensorMap& tK, const CUtensorMap& tV,
                         void* dk, void* dv, cudaStream_t st) {
-  auto kern = bf16 ? (p.compensated ? k_dkdv<true, true> : k_dkdv<true, false>)
-                   : (p.compensated ? k_dkdv<false, true> : k_dkdv<false, false>);
+  using Kern = decltype(&k_dkdv<true, false, false>);
+  static const Kern table[2][2][2] = {
+      {{k_dkdv<false, false, false>, k_dkdv<false, false, true>},
+       {k_dkdv<false, true, false>, k_dkdv<false, true, true>}},
+      {{k_dkdv<true, false, false>, k_dkdv<true, false, true>},
+       {k_dkdv<true, true, false>, k_dkdv<true, true, true>}}};
+  const Kern kern = table[bf16 ? 1 : 0][p.compensated ? 1 : 0][p.cu_q ? 1 : 0];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kv_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;
