@@ -402,8 +402,15 @@ TABLE_WORKLOADS = [
     ("blocksparse_bigbird_5000x7000", "hbm"),
     ("gqa_sink_varlen_causal_b8_s2048", "tensor"),
     ("gqa_sink_varlen_causal_b8_s2048_packed", "tensor"),
+    # the single-pass design (dq partials + fixed-order reduction) beside the
+    # split one, on the workloads whose walks are short
+    ("gqa_sink_swa128_s4096_single_pass", "hbm"),
+    ("blocksparse_random30_s8192_single_pass", "tensor"),
+    ("blocksparse_bigbird_5000x7000_single_pass", "hbm"),
+    ("gqa_sink_varlen_causal_b8_s2048_single_pass", "tensor"),
 ]
 PACKED_SUFFIX = "_packed"
+SINGLE_PASS_SUFFIX = "_single_pass"
 
 
 def time_workload(name, bound, device, peaks, min_steps=20, min_seconds=0.6, max_steps=2000):
@@ -413,14 +420,18 @@ def time_workload(name, bound, device, peaks, min_steps=20, min_seconds=0.6, max
     library's per-kernel events on."""
     from masked_attention_backward_gb300 import binding as mab
     packed = name.endswith(PACKED_SUFFIX)
-    wl = BY_NAME[name[:-len(PACKED_SUFFIX)] if packed else name]
+    single = name.endswith(SINGLE_PASS_SUFFIX)
+    base = name[:-len(PACKED_SUFFIX)] if packed else name
+    base = base[:-len(SINGLE_PASS_SUFFIX)] if single else base
+    wl = BY_NAME[base]
     inp, t = gpu_inputs(wl, device, packed=packed)
     pairs = measure.visible_pairs(wl, inp.block_mask, inp.seqlen_q, inp.seqlen_k)
     fl = measure.flops(wl, pairs)
     ab = measure.algorithmic_bytes(
         wl, 0 if inp.block_mask is None else int(inp.block_mask.numel()), inp.seqlen_q,
         inp.seqlen_k)
-    ws = mab.workspace(mab.shape_of(t["q"], t["k"], mask=t["mask"]), t["mask"], device)
+    flags = mab.ATTN_FLAG_SINGLE_PASS if single else 0
+    ws = mab.workspace(mab.shape_of(t["q"], t["k"], flags, mask=t["mask"]), t["mask"], device)
     out = (torch.empty_like(t["q"]), torch.empty_like(t["k"]), torch.empty_like(t["v"]),
            torch.empty_like(t["sink"]) if t["sink"] is not None else None)
     stream = torch.cuda.current_stream()
@@ -428,7 +439,7 @@ def time_workload(name, bound, device, peaks, min_steps=20, min_seconds=0.6, max
 
     def step():
         mab.bwd(t["q"], t["k"], t["v"], t["o"], t["dO"], t["lse"], t["sink"], t["mask"],
-                wl.scale, ws=ws, out=out)
+                wl.scale, ws=ws, out=out, single_pass=single)
 
     for _ in range(5):
         flush.zero_()
@@ -471,7 +482,11 @@ def time_workload(name, bound, device, peaks, min_steps=20, min_seconds=0.6, max
            "dtype": wl.dtype, "config": dict(workload_config(wl, pairs, fl, inp),
                                              **({"layout": "packed (token-major tensors, "
                                                            "cumulative sequence offsets)"}
-                                                if packed else {})),
+                                                if packed else {}),
+                                             **({"design": "single pass (dq partials in the "
+                                                           "workspace, fixed-order reduction)",
+                                                 "workspace_gb": round(ws.numel() / 1e9, 3)}
+                                                if single else {})),
            "clocks": clk}
     kd = {}
     for kname, v in kern.items():
@@ -482,6 +497,10 @@ def time_workload(name, bound, device, peaks, min_steps=20, min_seconds=0.6, max
             d["frac"] = round(d["tflops"] / tpk, 4)
         elif kname == "k_dq":
             d["tflops"] = round(fl["dq"] / (a * 1e-3) / 1e12, 1)
+            d["frac"] = round(d["tflops"] / tpk, 4)
+        elif kname == "k_dkdvq":
+            # all five contractions of the visible pairs
+            d["tflops"] = round(fl["total"] / (a * 1e-3) / 1e12, 1)
             d["frac"] = round(d["tflops"] / tpk, 4)
         elif kname == "k_preprocess":
             d["gbps"] = round(ab["preprocess"] / (a * 1e-3) / 1e9, 1)

@@ -77,8 +77,8 @@ typedef enum {
   ATTN_MASK_BLOCK = 3
 } attn_mask_kind_t;
 
-/* Shapes of one call; tensors are contiguous BHSD.  flags: 0 or
- * ATTN_FLAG_COMPENSATED. */
+/* Shapes of one call; tensors are contiguous BHSD.  flags: 0, or
+ * ATTN_FLAG_COMPENSATED or ATTN_FLAG_SINGLE_PASS (not both). */
 typedef struct {
   int B, Hq, Hkv, Sq, Skv, D;
   int dtype; /* attn_dtype_t */
@@ -91,7 +91,19 @@ typedef struct {
  * bits instead of 11 (fp16) or 8 (bf16) before the fp32 accumulation --
  * the compensated ("hi + lo") mode for tighter tolerances.  It costs 1.3x
  * the tensor work and 1.1x to 1.35x the time.  attn_fwd ignores it. */
-typedef enum { ATTN_FLAG_COMPENSATED = 1 } attn_flag_t;
+/* ATTN_FLAG_SINGLE_PASS (attn_bwd): the single-pass design of the backward.
+ * The key-stationary kernel also computes, for every visible (key tile,
+ * query sub-tile) step, that step's dq partial dS K in fp32 and stores it in
+ * the workspace; a second kernel sums each query sub-tile's partials in
+ * ascending key-tile order (deterministic) and rounds.  S and dP are then
+ * computed once per tile instead of twice (the default split design computes
+ * them again in its query-stationary dq kernel), at the price of 32 KB of
+ * partials written and read per step: the workspace grows by 32 KB + 1 byte
+ * per (query head, key tile, query sub-tile) step the key tiles can take at
+ * the full lengths (all of them for block masks).  Same results up to
+ * rounding order.  ATTN_ERR_UNSUPPORTED with ATTN_FLAG_COMPENSATED or the
+ * packed layout.  attn_fwd ignores it (its workspace need is unchanged). */
+typedef enum { ATTN_FLAG_COMPENSATED = 1, ATTN_FLAG_SINGLE_PASS = 2 } attn_flag_t;
 
 /* Mask description.  window is read for ATTN_MASK_SLIDING only; bx, by and
  * block_mask for ATTN_MASK_BLOCK only (block_mask is a device pointer).

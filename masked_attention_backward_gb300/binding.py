@@ -33,6 +33,7 @@ class attn_shape_t(ctypes.Structure):
 
 
 ATTN_FLAG_COMPENSATED = 1
+ATTN_FLAG_SINGLE_PASS = 2
 
 
 class attn_mask_desc_t(ctypes.Structure):
@@ -255,12 +256,16 @@ def fwd(q, k, v, sink, mask: Mask, scale: float, ws: Optional[torch.Tensor] = No
 
 
 def bwd(q, k, v, o, dO, lse, sink, mask: Mask, scale: float, ws: Optional[torch.Tensor] = None,
-        out=None, stream=None, compensated: bool = False):
+        out=None, stream=None, compensated: bool = False, single_pass: bool = False):
     """Backward; returns (dq, dk, dv, dsink) (dsink is None without a sink).
-    compensated: P and dS enter the contractions as high part + remainder."""
+    compensated: P and dS enter the contractions as high part + remainder.
+    single_pass: dq from partials of the key-stationary kernel, summed by a
+    reduction kernel (ATTN_FLAG_SINGLE_PASS) instead of the dq kernel."""
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dO, "dO"), (lse, "lse")):
         _check(t, n)
-    shape = shape_of(q, k, ATTN_FLAG_COMPENSATED if compensated else 0, mask=mask)
+    flags = (ATTN_FLAG_COMPENSATED if compensated else 0) | \
+        (ATTN_FLAG_SINGLE_PASS if single_pass else 0)
+    shape = shape_of(q, k, flags, mask=mask)
     if out is None:
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         dsink = torch.empty_like(sink) if sink is not None else None

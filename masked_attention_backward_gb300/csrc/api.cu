@@ -12,6 +12,8 @@
 //   k_dkdv              key-stationary dK / dV
 //   k_dq                query-stationary dQ
 //   k_dsink_finalize    sink only: dSink = -sum of partials
+// and with ATTN_FLAG_SINGLE_PASS k_dkdvq (dK / dV and the dQ partials) and
+// k_dq_reduce in place of k_dkdv and k_dq.
 #include <stdlib.h>
 #include <string.h>
 
@@ -38,7 +40,7 @@ attn_status_t check_shape_mask(const attn_shape_t* sh, const attn_mask_desc_t* m
     return ATTN_ERR_INVALID_ARG;
   if (sh->Hq % sh->Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (sh->dtype != ATTN_F16 && sh->dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
-  if (sh->flags & ~ATTN_FLAG_COMPENSATED) return ATTN_ERR_INVALID_ARG;
+  if (sh->flags & ~(ATTN_FLAG_COMPENSATED | ATTN_FLAG_SINGLE_PASS)) return ATTN_ERR_INVALID_ARG;
   // sequence lengths up to 2^24 and B*Hq up to 65535 keep every index and
   // grid dimension in range
   if (sh->Sq > (1 << 24) || sh->Skv > (1 << 24) || (long long)sh->B * sh->Hq > 65535)
@@ -69,7 +71,25 @@ attn_status_t check_shape_mask(const attn_shape_t* sh, const attn_mask_desc_t* m
       return ATTN_ERR_INVALID_ARG;
   }
   if (sh->D != HEAD_DIM) return ATTN_ERR_UNSUPPORTED;
+  // the single-pass kernels have neither the compensated nor the packed form
+  if ((sh->flags & ATTN_FLAG_SINGLE_PASS) &&
+      ((sh->flags & ATTN_FLAG_COMPENSATED) || mk->cu_seqlens_q))
+    return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
+}
+
+// Single pass: dq partial slots per query head (kv_tile_range_full summed over
+// the key tiles).
+long long single_pass_steps_head(const attn_shape_t* sh, const attn_mask_desc_t* mk) {
+  const int nKT = (sh->Skv + KV_TILE - 1) / KV_TILE;
+  const int kind = mk->kind;
+  const int window = kind == ATTN_MASK_SLIDING ? mk->window : 0;
+  long long n = 0;
+  for (int t = 0; t < nKT; ++t) {
+    int lo;
+    n += kv_tile_range_full(kind, window, sh->Sq, sh->Skv, t, &lo);
+  }
+  return n;
 }
 
 struct Dims {
@@ -115,6 +135,14 @@ WsLayout layout_of(const attn_shape_t* sh, const attn_mask_desc_t* mk) {
     off = align256(off + BH * d.nQT_q * d.nKT_q * sizeof(int));
     L.cnt_q = off;
     off = align256(off + BH * d.nQT_q * sizeof(int));
+  }
+  L.dq_flag = L.dq_part = off;
+  if (sh->flags & ATTN_FLAG_SINGLE_PASS) {
+    const size_t slots = BH * (size_t)single_pass_steps_head(sh, mk);
+    L.dq_flag = off;
+    off = align256(off + slots);
+    L.dq_part = off;
+    off = align256(off + slots * KV_SUB * HEAD_DIM * sizeof(float));
   }
   L.total = off;
   return L;
@@ -176,6 +204,11 @@ AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const W
   p.timeout_ns = wait_timeout_ns();
   p.test_no_loads = test_no_loads();
   p.compensated = (sh->flags & ATTN_FLAG_COMPENSATED) ? 1 : 0;
+  if (sh->flags & ATTN_FLAG_SINGLE_PASS) {
+    p.dq_part = reinterpret_cast<float*>(ws + L.dq_part);
+    p.dq_flag = ws + L.dq_flag;
+    p.dq_steps_head = single_pass_steps_head(sh, mk);
+  }
   p.seqlen_q = mk->seqlen_q;
   p.seqlen_k = mk->seqlen_k;
   if (mk->cu_seqlens_q) {
@@ -296,6 +329,10 @@ attn_status_t attn_fwd(const attn_shape_t* shape, const void* q, const void* k, 
       !aligned(lse, 4) || !aligned(ws, 256) || (sink && !aligned(sink, 4)))
     return ATTN_ERR_INVALID_ARG;
   if (mask->kind == ATTN_MASK_BLOCK && !mask->block_mask) return ATTN_ERR_INVALID_ARG;
+  // the forward needs none of the backward's single-pass regions
+  attn_shape_t fsh = *shape;
+  fsh.flags &= ~ATTN_FLAG_SINGLE_PASS;
+  shape = &fsh;
   const WsLayout L = layout_of(shape, mask);
   if (ws_bytes < L.total) return ATTN_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -357,9 +394,13 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
       !make_map(&tVs, v, bf16, shape, mask, false, Q_SUB))
     return ATTN_ERR_CUDA;
 
+  const bool single = (shape->flags & ATTN_FLAG_SINGLE_PASS) != 0;
+
   std::unique_lock<std::mutex> lock(g_prof.mu, std::defer_lock);
   const bool prof = prof_lock(lock);
   cudaError_t e = cudaMemsetAsync(w + L.status, 0, sizeof(DevStatus), st);
+  if (e == cudaSuccess && single)
+    e = cudaMemsetAsync(w + L.dq_flag, 0, L.dq_part - L.dq_flag, st);
   if (e == cudaSuccess) {
     ProfScope ps(prof, "k_preprocess", st);
     e = launch_preprocess(bf16, o, dO, lse, sink, reinterpret_cast<float*>(w + L.nlse2),
@@ -372,13 +413,24 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
     ProfScope ps(prof, "k_mask_tables", st);
     e = enqueue_tables(shape, L, w, p, st);
   }
-  if (e == cudaSuccess) {
-    ProfScope ps(prof, "k_dkdv", st);
-    e = launch_dkdv(bf16, p, tQs, tdOs, tKt, tVt, dk, dv, st);
-  }
-  if (e == cudaSuccess) {
-    ProfScope ps(prof, "k_dq", st);
-    e = launch_dq(bf16, p, tQt, tdOt, tKs, tVs, dq, st);
+  if (e == cudaSuccess && single) {
+    {
+      ProfScope ps(prof, "k_dkdvq", st);
+      e = launch_dkdvq(bf16, p, tQs, tdOs, tKt, tVt, dk, dv, st);
+    }
+    if (e == cudaSuccess) {
+      ProfScope ps(prof, "k_dq_reduce", st);
+      e = launch_dq_reduce(bf16, p, dq, st);
+    }
+  } else if (e == cudaSuccess) {
+    {
+      ProfScope ps(prof, "k_dkdv", st);
+      e = launch_dkdv(bf16, p, tQs, tdOs, tKt, tVt, dk, dv, st);
+    }
+    if (e == cudaSuccess) {
+      ProfScope ps(prof, "k_dq", st);
+      e = launch_dq(bf16, p, tQt, tdOt, tKs, tVs, dq, st);
+    }
   }
   if (e == cudaSuccess && sink) {
     ProfScope ps(prof, "k_dsink_finalize", st);

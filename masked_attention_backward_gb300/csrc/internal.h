@@ -34,6 +34,8 @@ struct WsLayout {
   size_t cnt_k;      // int32 [B*Hq, nKT_k]
   size_t sel_q;      // int32 [B*Hq, nQT_q, nKT_q]  (query tiles of Q_TILE, key tiles of Q_SUB)
   size_t cnt_q;      // int32 [B*Hq, nQT_q]
+  size_t dq_flag;    // single pass: uint8 [B*Hq, steps per head], 1 = partial written
+  size_t dq_part;    // single pass: float [B*Hq, steps per head, KV_SUB, HEAD_DIM]
   size_t total;
 };
 
@@ -69,6 +71,13 @@ struct AttnParams {
   const int* cu_q;
   const int* cu_k;
   int total_q, total_k;
+  // Single pass: the dq partial of each step of the dK/dV walk and its
+  // written flag.  Slots of one query head: key tile t's steps follow those of
+  // the tiles before it, query sub-tile r of the tile at (r - its range's
+  // first sub-tile), over the full-length ranges (kv_tile_range_full).
+  float* dq_part;
+  uint8_t* dq_flag;
+  long long dq_steps_head;  // slots per query head
 };
 
 #ifdef __CUDACC__
@@ -185,5 +194,28 @@ __host__ __device__ inline void partner_range(int kind, int window, bool own_is_
   *lo = (int)(a / psize);
   *hi = (int)(b / psize);
 }
+
+// Query sub-tiles of KV_SUB rows key tile t (KV_TILE keys) can meet at the
+// full lengths: the partner range of the closed-form masks (first sub-tile in
+// *lo), or all of them for block masks (*lo = 0).  Shorter per-batch lengths
+// only cut a range's end, so these ranges hold every step of any walk.
+__host__ __device__ inline int kv_tile_range_full(int kind, int window, int Sq, int Skv, int t,
+                                                  int* lo) {
+  const int nQT = (Sq + KV_SUB - 1) / KV_SUB;
+  if (kind == MK_BLOCK) {
+    *lo = 0;
+    return nQT;
+  }
+  const int k0 = t * KV_TILE;
+  const int k1 = k0 + KV_TILE < Skv ? k0 + KV_TILE : Skv;
+  int hi;
+  partner_range(kind, window, false, k0, k1, KV_SUB, Sq, lo, &hi);
+  return hi >= *lo ? hi - *lo + 1 : 0;
+}
+
+cudaError_t launch_dkdvq(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
+                         const CUtensorMap& tdO, const CUtensorMap& tK, const CUtensorMap& tV,
+                         void* dk, void* dv, cudaStream_t st);
+cudaError_t launch_dq_reduce(bool bf16, const AttnParams& p, void* dq, cudaStream_t st);
 
 }  // namespace mab

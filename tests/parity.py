@@ -16,7 +16,8 @@ import torch
 
 import oracle
 from masked_attention_backward_gb300 import binding as mab
-from masked_attention_backward_gb300.workloads import MASK_BLOCK, Inputs, Workload, make_inputs
+from masked_attention_backward_gb300.workloads import (MASK_BLOCK, MASK_NONE, MASK_SLIDING, Inputs,
+                                                        Workload, make_inputs)
 
 TOL = {"f16": 2e-3, "bf16": 1.6e-2}
 MIN_FRAC = 0.999
@@ -105,7 +106,7 @@ class GpuRun:
 
 
 def run_gpu_bwd(wl: Workload, inp: Inputs, O, lse, poison: bool = True,
-                compensated: bool = False) -> GpuRun:
+                compensated: bool = False, single_pass: bool = False) -> GpuRun:
     dev = "cuda"
     q, k, v, dO = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.dO))
     o, l = O.to(dev), lse.to(dev)
@@ -118,21 +119,22 @@ def run_gpu_bwd(wl: Workload, inp: Inputs, O, lse, poison: bool = True,
             t.fill_(float("nan"))
         if dsink is not None:
             dsink.fill_(float("nan"))
-    ws = mab.workspace(mab.shape_of(q, k), mask, dev)
+    flags = mab.ATTN_FLAG_SINGLE_PASS if single_pass else 0
+    ws = mab.workspace(mab.shape_of(q, k, flags), mask, dev)
     mab.bwd(q, k, v, o, dO, l, sink, mask, wl.scale, ws=ws, out=(dq, dk, dv, dsink),
-            compensated=compensated)
+            compensated=compensated, single_pass=single_pass)
     torch.cuda.synchronize()
     st = mab.device_status(ws)
     assert st == mab.ATTN_OK, mab.attn_status_string(st)
     return GpuRun(dq, dk, dv, dsink, ws)
 
 
-def full_parity(wl: Workload, seed=None):
+def full_parity(wl: Workload, seed=None, single_pass: bool = False):
     """Element-by-element parity of dq, dk, dv (and dsink) against the oracle."""
     inp = make_inputs(wl, seed)
     pb = oracle_problem(wl, inp)
     O, lse = forward_stats(wl, inp, pb)
-    run = run_gpu_bwd(wl, inp, O, lse)
+    run = run_gpu_bwd(wl, inp, O, lse, single_pass=single_pass)
     ref = oracle.backward(pb, inp.q, inp.k, inp.v, O, inp.dO, lse)
     reps = [compare("dq", run.dq, ref["dq"], wl.dtype),
             compare("dk", run.dk, ref["dk"], wl.dtype),
@@ -153,7 +155,32 @@ def _a256(x):
     return (x + 255) // 256 * 256
 
 
-def ws_layout(wl: Workload) -> dict:
+def tile_pair_visible(wl: Workload, i0: int, i1: int, j0: int, j1: int) -> bool:
+    """Whether query rows [i0, i1) and keys [j0, j1) hold a visible pair under
+    a closed-form mask: causal j <= i, sliding window 0 <= i - j < W, or none.
+    The differences i - j the two ranges can form are [i0 - (j1 - 1),
+    (i1 - 1) - j0]; a pair is visible when that interval meets the mask's."""
+    if wl.mask_kind == MASK_NONE:
+        return True
+    lo, hi = i0 - (j1 - 1), (i1 - 1) - j0
+    w = wl.window if wl.mask_kind == MASK_SLIDING else 1 << 40
+    return hi >= 0 and lo <= w - 1
+
+
+def single_pass_steps_head(wl: Workload) -> int:
+    """dq partial slots per query head of the single-pass backward: the
+    (key tile, query sub-tile) pairs holding a visible pair at the full
+    lengths, every pair for block masks."""
+    cdiv = lambda a, b: -(-a // b)
+    nkt, nqt = cdiv(wl.Skv, KV_TILE), cdiv(wl.Sq, KV_SUB)
+    if wl.mask_kind == MASK_BLOCK:
+        return nkt * nqt
+    return sum(tile_pair_visible(wl, r * KV_SUB, min((r + 1) * KV_SUB, wl.Sq), t * KV_TILE,
+                                 min((t + 1) * KV_TILE, wl.Skv))
+               for t in range(nkt) for r in range(nqt))
+
+
+def ws_layout(wl: Workload, single_pass: bool = False) -> dict:
     cdiv = lambda a, b: -(-a // b)
     Sq_pad = cdiv(wl.Sq, PREP_ROWS) * PREP_ROWS
     BH = wl.B * wl.Hq
@@ -170,6 +197,10 @@ def ws_layout(wl: Workload) -> dict:
         L["cnt_k"] = off; off = _a256(off + BH * d["nKT_k"] * 4)
         L["sel_q"] = off; off = _a256(off + BH * d["nQT_q"] * d["nKT_q"] * 4)
         L["cnt_q"] = off; off = _a256(off + BH * d["nQT_q"] * 4)
+    if single_pass:
+        slots = BH * single_pass_steps_head(wl)
+        L["dq_flag"] = off; off = _a256(off + slots)
+        L["dq_part"] = off; off = _a256(off + slots * KV_SUB * 128 * 4)
     L["total"] = off
     L.update(d)
     return L

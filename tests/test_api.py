@@ -49,7 +49,14 @@ def test_status_strings(lib):
     (_shape(), mab.attn_mask_desc_t(3, 0, 0, 16, None), mab.ATTN_ERR_INVALID_ARG),
     (_shape(), mab.attn_mask_desc_t(7, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
     (_shape(dtype=5), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
-    (_shape(flags=2), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(flags=4), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
+    (_shape(flags=mab.ATTN_FLAG_SINGLE_PASS), mab.attn_mask_desc_t(1, 0, 1, 1, None), mab.ATTN_OK),
+    # the single-pass kernels have no compensated and no packed form
+    (_shape(flags=mab.ATTN_FLAG_SINGLE_PASS | mab.ATTN_FLAG_COMPENSATED),
+     mab.attn_mask_desc_t(1, 0, 1, 1, None), mab.ATTN_ERR_UNSUPPORTED),
+    (_shape(flags=mab.ATTN_FLAG_SINGLE_PASS),
+     mab.attn_mask_desc_t(0, 0, 1, 1, None, None, None, 4096, 8192, 100, 90),
+     mab.ATTN_ERR_UNSUPPORTED),
     (_shape(flags=-1), mab.attn_mask_desc_t(0, 0, 1, 1, None), mab.ATTN_ERR_INVALID_ARG),
     (_shape(flags=mab.ATTN_FLAG_COMPENSATED), mab.attn_mask_desc_t(1, 0, 1, 1, None), mab.ATTN_OK),
     (_shape(B=1024, Hq=128, Hkv=128), mab.attn_mask_desc_t(0, 0, 1, 1, None),
@@ -88,6 +95,35 @@ def test_workspace_size_matches_layout(lib):
         r, n = mab.attn_workspace_size(shape, mask)
         assert r == mab.ATTN_OK
         assert n == ws_layout(wl)["total"], wl.name
+
+
+def test_single_pass_workspace_size(lib):
+    """The single-pass regions: one flag byte and one 64 x 128 fp32 partial
+    per (query head, key tile, query sub-tile) pair that holds a visible pair
+    (counted from the mask's definition), every pair for block masks."""
+    from parity import single_pass_steps_head, ws_layout
+    from masked_attention_backward_gb300.workloads import Workload
+    extra = [
+        Workload("causal_ragged", "bf16", B=2, Hq=4, Hkv=2, Sq=333, Skv=333, mask_kind=1),
+        Workload("swa1", "f16", B=1, Hq=2, Hkv=1, Sq=300, Skv=300, mask_kind=2, window=1),
+        Workload("swa100", "bf16", B=1, Hq=2, Hkv=1, Sq=1000, Skv=1000, mask_kind=2, window=100),
+        Workload("dense_uneven", "f16", B=1, Hq=2, Hkv=1, Sq=200, Skv=333, mask_kind=0),
+    ]
+    for wl in list(WORKLOADS) + extra:
+        flags = mab.ATTN_FLAG_SINGLE_PASS
+        shape = mab.attn_shape_t(wl.B, wl.Hq, wl.Hkv, wl.Sq, wl.Skv, wl.D,
+                                 mab.ATTN_F16 if wl.dtype == "f16" else mab.ATTN_BF16, flags)
+        mask = mab.attn_mask_desc_t(wl.mask_kind, wl.window, wl.bx, wl.by, None)
+        r, n = mab.attn_workspace_size(shape, mask)
+        assert r == mab.ATTN_OK
+        L = ws_layout(wl, single_pass=True)
+        assert n == L["total"], wl.name
+        assert L["total"] - ws_layout(wl)["total"] >= \
+            wl.B * wl.Hq * single_pass_steps_head(wl) * (64 * 128 * 4 + 1)
+    # the causal count in closed form: key tile t meets the sub-tiles from 2t on
+    wl = WORKLOADS[4]
+    nkt, nqt = wl.Skv // 128, wl.Sq // 64
+    assert single_pass_steps_head(wl) == sum(nqt - 2 * t for t in range(nkt))
 
 
 def _bwd(shape, mask, ws_bytes=1 << 30, **over):
