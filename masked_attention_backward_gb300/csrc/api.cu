@@ -6,14 +6,15 @@
 // runbook, optimisation 1: the host does shape, alloc and view only).
 //
 // attn_bwd enqueues, in order:
-//   k_preprocess        Delta, lse*log2(e) (padded), dSink partials
-//   k_mask_transpose +  block masks only: transposed mask and both
-//   k_build_sel           select tables
-//   k_dkdv              key-stationary dK / dV
+//   k_mask_tables       block masks only: transposed mask and both select
+//                         tables
+//   k_preprocess        Delta, lse*log2(e) (padded), dSink partials (beside
+//                         the tables)
+//   k_dkdv              key-stationary dK / dV; with a sink its last CTA
+//                         sums dSink = -(sum of the partials)
 //   k_dq                query-stationary dQ
-//   k_dsink_finalize    sink only: dSink = -sum of partials
-// and with ATTN_FLAG_SINGLE_PASS k_dkdvq (dK / dV and the dQ partials) and
-// k_dq_reduce in place of k_dkdv and k_dq.
+// and with ATTN_FLAG_SINGLE_PASS k_dkdvq (dK / dV and the dQ partials),
+// k_dq_reduce and k_dsink_finalize (sink only) in place of k_dkdv and k_dq.
 #include <stdlib.h>
 #include <string.h>
 
@@ -283,15 +284,12 @@ bool prof_lock(std::unique_lock<std::mutex>& lock) {
   return true;
 }
 
-// Transposed mask and both select tables (block masks only).
-cudaError_t enqueue_tables(const attn_shape_t* sh, const WsLayout& L, uint8_t* ws,
-                           const AttnParams& p, cudaStream_t st) {
-  cudaError_t e = launch_mask_transpose(p.mask, ws + L.maskT, sh->B * sh->Hq, p.nqb, p.nkb, st);
-  if (e != cudaSuccess) return e;
-  return launch_build_sel(p, reinterpret_cast<int*>(ws + L.sel_k),
-                          reinterpret_cast<int*>(ws + L.cnt_k),
-                          reinterpret_cast<int*>(ws + L.sel_q),
-                          reinterpret_cast<int*>(ws + L.cnt_q), st);
+// Transposed mask and both select tables (block masks only), one launch.
+cudaError_t enqueue_tables(const WsLayout& L, uint8_t* ws, const AttnParams& p, cudaStream_t st) {
+  return launch_mask_tables(p, ws + L.maskT, reinterpret_cast<int*>(ws + L.sel_k),
+                            reinterpret_cast<int*>(ws + L.cnt_k),
+                            reinterpret_cast<int*>(ws + L.sel_q),
+                            reinterpret_cast<int*>(ws + L.cnt_q), st);
 }
 
 }  // namespace
@@ -351,7 +349,7 @@ attn_status_t attn_fwd(const attn_shape_t* shape, const void* q, const void* k, 
   cudaError_t e = cudaMemsetAsync(w + L.status, 0, sizeof(DevStatus), st);
   if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) {
     ProfScope ps(prof, "k_mask_tables", st);
-    e = enqueue_tables(shape, L, w, p, st);
+    e = enqueue_tables(L, w, p, st);
   }
   if (e == cudaSuccess) {
     ProfScope ps(prof, "k_attn_fwd", st);
@@ -401,17 +399,20 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
   cudaError_t e = cudaMemsetAsync(w + L.status, 0, sizeof(DevStatus), st);
   if (e == cudaSuccess && single)
     e = cudaMemsetAsync(w + L.dq_flag, 0, L.dq_part - L.dq_flag, st);
+  // block masks: the tables first, and the preprocess grid beside them (it
+  // reads nothing of theirs; its completion implies theirs)
+  const bool blk = mask->kind == ATTN_MASK_BLOCK;
+  if (e == cudaSuccess && blk) {
+    ProfScope ps(prof, "k_mask_tables", st);
+    e = enqueue_tables(L, w, p, st);
+  }
   if (e == cudaSuccess) {
     ProfScope ps(prof, "k_preprocess", st);
     e = launch_preprocess(bf16, o, dO, lse, sink, reinterpret_cast<float*>(w + L.nlse2),
                           reinterpret_cast<float*>(w + L.delta),
                           reinterpret_cast<float*>(w + L.dsink_part), shape->B, shape->Hq,
                           shape->Sq, d.Sq_pad, mask->seqlen_q, mask->cu_seqlens_q,
-                          mask->total_q, st);
-  }
-  if (e == cudaSuccess && mask->kind == ATTN_MASK_BLOCK) {
-    ProfScope ps(prof, "k_mask_tables", st);
-    e = enqueue_tables(shape, L, w, p, st);
+                          mask->total_q, blk && !prof, st);
   }
   if (e == cudaSuccess && single) {
     {
@@ -423,6 +424,12 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
       e = launch_dq_reduce(bf16, p, dq, st);
     }
   } else if (e == cudaSuccess) {
+    // the dK/dV grid's last CTA also sums dSink
+    if (sink) {
+      p.dsink = dsink;
+      p.dsink_part = reinterpret_cast<const float*>(w + L.dsink_part);
+      p.dsink_nparts = d.nparts;
+    }
     {
       ProfScope ps(prof, "k_dkdv", st);
       e = launch_dkdv(bf16, p, tQs, tdOs, tKt, tVt, dk, dv, st);
@@ -432,7 +439,7 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
       e = launch_dq(bf16, p, tQt, tdOt, tKs, tVs, dq, st);
     }
   }
-  if (e == cudaSuccess && sink) {
+  if (e == cudaSuccess && sink && single) {
     ProfScope ps(prof, "k_dsink_finalize", st);
     e = launch_dsink_finalize(reinterpret_cast<const float*>(w + L.dsink_part), shape->Hq,
                               d.nparts, dsink, st);

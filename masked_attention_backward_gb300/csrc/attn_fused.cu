@@ -126,6 +126,9 @@ k_dkdvq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
   const int b = bc / p.Hkv, c = bc % p.Hkv;
   const int k0 = t * KV_TILE;
   const int Lq = len_q(p, b), Lk = len_k(p, b);
+  // block masks: the walk reads the select tables, which the grids before
+  // this one (launched with programmatic serialization) are still writing
+  if (p.mask_kind == MK_BLOCK) grid_dependency_wait();
   KVWalk walk;
   walk.init(p, b, c, t, Lq, Lk);
   const int N = walk.total(p);
@@ -561,8 +564,8 @@ cudaError_t launch_dkdvq(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                                        (int)fused_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int nKT = (p.Skv + KV_TILE - 1) / KV_TILE;
-  // closed-form masks: programmatic serialization behind the preprocess
-  // kernel (block masks read the select tables as soon as a CTA starts)
+  // programmatic serialization behind the preprocess kernel (block-mask CTAs
+  // wait for it before they read the select tables)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(nKT * p.B * p.Hkv));
   cfg.blockDim = dim3(fused_side::NUM_THREADS);
@@ -572,7 +575,7 @@ cudaError_t launch_dkdvq(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = p.mask_kind == MK_BLOCK ? 0 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tQ, tdO, tK, tV, (uint16_t*)dk, (uint16_t*)dv, p);
 }
 

@@ -84,6 +84,7 @@ struct __align__(1024) Smem {
   uint64_t bar_acc_full;         // every dV and dK MMA complete (one commit each)
   uint32_t tmem_base;
   int abort_flag;
+  int is_last;                   // this CTA finished last: it sums dSink
 };
 
 constexpr size_t SMEM_BYTES = sizeof(Smem) + 1024;
@@ -117,6 +118,9 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
   const int b = bc / p.Hkv, c = bc % p.Hkv;
   const int k0 = t * KV_TILE;
   const int Lq = len_q(p, b), Lk = len_k(p, b);  // valid rows and keys of the batch
+  // block masks: the walk reads the select tables, which the grids before
+  // this one (launched with programmatic serialization) are still writing
+  if (p.mask_kind == MK_BLOCK) grid_dependency_wait();
   KVWalk walk;
   walk.init(p, b, c, t, Lq, Lk);
   const int N = walk.total(p);
@@ -166,9 +170,9 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = s.tmem_base;
-  // Launched behind the preprocess kernel with programmatic serialization
-  // (closed-form masks), this grid may start before that one has finished:
-  // wait for it before any of its results are read.  Only then let the dQ
+  // Launched behind the preprocess kernel with programmatic serialization,
+  // this grid may start before that one has finished: wait for it before any
+  // of its results are read (block masks waited above already).  Only then let the dQ
   // kernel that follows start (it needs nothing from this grid, but reads the
   // preprocess results): it may take the SMs this grid's last CTAs leave idle.
   grid_dependency_wait();
@@ -496,6 +500,18 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
     tc_fence_after();
     tmem_dealloc(tbase, 512);
   }
+  // dSink by the grid's last CTA, off the critical path of the dQ grid that
+  // runs beside this one's tail (the partials come from the preprocess grid,
+  // which every CTA waited for above)
+  if (p.dsink) {
+    if (threadIdx.x == 0) s.is_last = atomicAdd(&p.status->kv_done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (s.is_last)
+      for (int h = warp; h < p.Hq; h += NUM_THREADS / 32) {
+        const float v = dsink_of_head(p.dsink_part, p.dsink_nparts, h, lane);
+        if (lane == 0) p.dsink[h] = v;
+      }
+  }
 }
 
 cudaError_t launch_dkdv(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
@@ -512,10 +528,9 @@ cudaError_t launch_dkdv(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                                        (int)kv_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const int nKT = (p.Skv + KV_TILE - 1) / KV_TILE;
-  // closed-form masks: programmatic stream serialization behind the
-  // preprocess kernel, so that this grid's set-up and K / V loads overlap its
-  // tail (block masks read the select tables as soon as a CTA starts, so the
-  // table kernels before them must have completed)
+  // programmatic stream serialization behind the preprocess kernel, so that
+  // this grid's launch and (closed-form masks) set-up and K / V loads overlap
+  // its tail; block-mask CTAs wait for it before they read the select tables
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(nKT * p.B * p.Hkv));
   cfg.blockDim = dim3(kv_side::NUM_THREADS);
@@ -525,7 +540,7 @@ cudaError_t launch_dkdv(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = p.mask_kind == MK_BLOCK ? 0 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tQ, tdO, tK, tV, (uint16_t*)dk, (uint16_t*)dv, p);
 }
 

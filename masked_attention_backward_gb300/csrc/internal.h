@@ -71,6 +71,12 @@ struct AttnParams {
   const int* cu_q;
   const int* cu_k;
   int total_q, total_k;
+  // dSink, summed from the preprocess kernel's partials ([Hq, nparts]) by the
+  // dK/dV grid's last CTA; nullptr when that grid does not (no sink, or the
+  // single-pass kernels, which leave it to k_dsink_finalize).
+  float* dsink;
+  const float* dsink_part;
+  int dsink_nparts;
   // Single pass: the dq partial of each step of the dK/dV walk and its
   // written flag.  Slots of one query head: key tile t's steps follow those of
   // the tiles before it, query sub-tile r of the tile at (r - its range's
@@ -89,6 +95,16 @@ __device__ __forceinline__ int packed_off(const int* cu, int b, int total) {
 __device__ __forceinline__ int packed_len(const int* cu, int b, int total, int smax) {
   const int o = packed_off(cu, b, total);
   return min(min(max(cu[b + 1], o), total) - o, smax);
+}
+
+// -(sum of head h's dSink partials), summed by one warp in a fixed order
+// (lane-strided in fp64, then a butterfly): every caller gets the same bits.
+__device__ __forceinline__ float dsink_of_head(const float* part, int nparts, int h, int lane) {
+  double s = 0.0;
+  for (int i = lane; i < nparts; i += 32) s += (double)part[(size_t)h * nparts + i];
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  return (float)(-s);
 }
 
 // Valid query rows / keys of batch b: the per-batch lengths clamped to
@@ -142,13 +158,11 @@ __device__ __forceinline__ int rows_to_store_k(const AttnParams& p, int b, int r
 cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const float* lse,
                               const float* sink, float* nlse2, float* delta, float* part, int B,
                               int Hq, int Sq, int Sq_pad, const int* seqlen_q, const int* cu_q,
-                              int total_q, cudaStream_t st);
+                              int total_q, bool overlap_prev, cudaStream_t st);
 cudaError_t launch_dsink_finalize(const float* part, int Hq, int nparts, float* dsink,
                                   cudaStream_t st);
-cudaError_t launch_mask_transpose(const uint8_t* mask, uint8_t* maskT, int BH, int nqb, int nkb,
-                                  cudaStream_t st);
-cudaError_t launch_build_sel(const AttnParams& p, int* sel_k, int* cnt_k, int* sel_q, int* cnt_q,
-                             cudaStream_t st);
+cudaError_t launch_mask_tables(const AttnParams& p, uint8_t* maskT, int* sel_k, int* cnt_k,
+                               int* sel_q, int* cnt_q, cudaStream_t st);
 cudaError_t launch_dkdv(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                         const CUtensorMap& tdO, const CUtensorMap& tK, const CUtensorMap& tV,
                         void* dk, void* dv, cudaStream_t st);

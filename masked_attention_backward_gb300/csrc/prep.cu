@@ -2,9 +2,10 @@
 //   k_preprocess      Delta = rowsum(dO * O), nlse2 = -lse * log2(e) (padded),
 //                     and per-block partial sums of exp(sink - lse) * Delta;
 //   k_dsink_finalize  dSink_h = -(fixed-order sum of the partials);
-//   k_mask_transpose  uint8 block mask [BH,nQB,nKB] -> [BH,nKB,nQB];
-//   k_build_sel       select tables: per key tile the ascending list of query
-//                     sub-tiles that share an active block, and vice versa.
+//   k_mask_tables     uint8 block mask [BH,nQB,nKB] -> [BH,nKB,nQB] (transpose)
+//                     and the select tables: per key tile the ascending list
+//                     of query sub-tiles that share an active block, and vice
+//                     versa (one launch).
 //
 // Sources: tilelang-ascend PR #1 "Add GQA Sink Backward BHSD", commit notes of
 // the 2-kernel design (Phase0 Delta = sum(O*dO); Phase5 dSink);
@@ -109,49 +110,47 @@ k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
       part[(size_t)h * nparts + (size_t)b * gridDim.x + blk] = s;
     }
   }
+  // Behind the mask-table kernel (block masks) this grid is launched with
+  // programmatic serialization and runs beside it: one thread keeps this grid
+  // from completing before that one has, so the kernels waiting for this
+  // grid see both complete (a no-op after an ordinary launch).
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) grid_dependency_wait();
 }
 
 __global__ void k_dsink_finalize(const float* __restrict__ part, int nparts,
                                  float* __restrict__ dsink) {
   const int h = blockIdx.x, lane = threadIdx.x;
-  double s = 0.0;
-  for (int i = lane; i < nparts; i += 32) s += (double)part[(size_t)h * nparts + i];
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) dsink[h] = (float)(-s);
+  const float v = dsink_of_head(part, nparts, h, lane);
+  if (lane == 0) dsink[h] = v;
 }
 
-// 32x32 byte tiles through shared memory.
-__global__ void k_mask_transpose(const uint8_t* __restrict__ mask, uint8_t* __restrict__ maskT,
-                                 int BH, int nqb, int nkb) {
+// Transpose of one 32 x 32 tile of query blocks x key blocks of one (b, h)
+// through shared memory (128 threads: 32 columns x 4 rows at a time).
+__device__ void transpose_tile(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int nqb,
+                               int nkb, int qb0, int kb0) {
   __shared__ uint8_t tile[32][33];
-  const int kb0 = blockIdx.x * 32, qb0 = blockIdx.y * 32;
-  for (int bh = blockIdx.z; bh < BH; bh += gridDim.z) {
-    const uint8_t* src = mask + (size_t)bh * nqb * nkb;
-    uint8_t* dst = maskT + (size_t)bh * nqb * nkb;
-    for (int r = threadIdx.y; r < 32; r += blockDim.y) {
-      int qb = qb0 + r, kb = kb0 + threadIdx.x;
-      if (qb < nqb && kb < nkb) tile[r][threadIdx.x] = src[(size_t)qb * nkb + kb];
-    }
-    __syncthreads();
-    for (int r = threadIdx.y; r < 32; r += blockDim.y) {
-      int kb = kb0 + r, qb = qb0 + threadIdx.x;
-      if (qb < nqb && kb < nkb) dst[(size_t)kb * nqb + qb] = tile[threadIdx.x][r];
-    }
-    __syncthreads();
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int r = ty; r < 32; r += 4) {
+    const int qb = qb0 + r, kb = kb0 + tx;
+    if (qb < nqb && kb < nkb) tile[r][tx] = src[(size_t)qb * nkb + kb];
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 4) {
+    const int kb = kb0 + r, qb = qb0 + tx;
+    if (qb < nqb && kb < nkb) dst[(size_t)kb * nqb + qb] = tile[tx][r];
   }
 }
 
 // One warp per table row.  The row's own tile covers [o0, o1) on its axis;
 // candidate partner tile t covers [t*psize, min((t+1)*psize, plen)).  A pair
 // is active when some mask block with a nonzero byte overlaps both ranges.
-// `rows` points at the mask rows of this (b,h) laid out [own block][partner
-// block] (maskT for key-major walks, the mask itself for query-major walks),
-// so each probe reads a contiguous run of bytes.  Entries are written at the
-// exclusive prefix count of active candidates (warp ballot + popc).
-__device__ void build_row(const uint8_t* __restrict__ rows, int npb, int own_bs, int part_bs,
-                          int o0, int o1, int psize, int plen, int* __restrict__ sel_row,
-                          int nP, int* __restrict__ cnt) {
+// The mask byte of (own block ob, partner block pb) is
+// m[ob * own_stride + pb * part_stride] (the (b, h) mask read along either
+// axis).  Entries are written at the exclusive prefix count of active
+// candidates (warp ballot + popc).
+__device__ void build_row(const uint8_t* __restrict__ m, size_t own_stride, size_t part_stride,
+                          int own_bs, int part_bs, int o0, int o1, int psize, int plen,
+                          int* __restrict__ sel_row, int nP, int* __restrict__ cnt) {
   const int lane = threadIdx.x & 31;
   const int ob_lo = o0 / own_bs, ob_hi = (o1 - 1) / own_bs;
   int n = 0;
@@ -162,9 +161,9 @@ __device__ void build_row(const uint8_t* __restrict__ rows, int npb, int own_bs,
       int p0 = t * psize, p1 = min(p0 + psize, plen);
       int pb_lo = p0 / part_bs, pb_hi = (p1 - 1) / part_bs;
       for (int ob = ob_lo; ob <= ob_hi && !act; ++ob) {
-        const uint8_t* r = rows + (size_t)ob * npb;
+        const uint8_t* r = m + (size_t)ob * own_stride;
         for (int pb = pb_lo; pb <= pb_hi; ++pb)
-          if (r[pb]) {
+          if (r[(size_t)pb * part_stride]) {
             act = true;
             break;
           }
@@ -178,23 +177,37 @@ __device__ void build_row(const uint8_t* __restrict__ rows, int npb, int own_bs,
   if (lane == 0) *cnt = n;
 }
 
-// grid.x covers rows of both tables: first BH*nKT_k key-major rows, then
-// BH*nQT_q query-major rows; 4 warps per block.
-__global__ void k_build_sel(AttnParams p, int* __restrict__ sel_k, int* __restrict__ cnt_k,
-                            int* __restrict__ sel_q, int* __restrict__ cnt_q) {
-  const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
+// Both mask steps in one launch of 128-thread blocks: the first n_tr blocks
+// transpose the mask (32 x 32 tiles; the key-stationary kernels read the
+// transposed rows), the rest build the select tables, one warp per row: first
+// BH*nKT_k key-major rows, then BH*nQT_q query-major rows.  The tables read
+// the mask itself along either axis, so neither part waits for the other.
+__global__ void __launch_bounds__(128)
+k_mask_tables(const AttnParams p, uint8_t* __restrict__ maskT, int n_tr, int* __restrict__ sel_k,
+              int* __restrict__ cnt_k, int* __restrict__ sel_q, int* __restrict__ cnt_q) {
+  // the preprocess grid behind this one reads nothing of it: let it start
+  grid_launch_dependents();
   const int BH = p.B * p.Hq;
+  const size_t per_head = (size_t)p.nqb * p.nkb;
+  if ((int)blockIdx.x < n_tr) {
+    const int tk = (p.nkb + 31) / 32, tq = (p.nqb + 31) / 32;
+    const int bh = blockIdx.x / (tk * tq), rem = blockIdx.x % (tk * tq);
+    transpose_tile(p.mask + bh * per_head, maskT + bh * per_head, p.nqb, p.nkb, (rem / tk) * 32,
+                   (rem % tk) * 32);
+    return;
+  }
+  const int gw = (blockIdx.x - n_tr) * 4 + (threadIdx.x >> 5);
   const int nk_rows = BH * p.nKT_k;
   if (gw < nk_rows) {
     int bh = gw / p.nKT_k, kt = gw % p.nKT_k;
     int o0 = kt * KV_TILE, o1 = min(o0 + KV_TILE, p.Skv);
-    build_row(p.maskT + (size_t)bh * p.nkb * p.nqb, p.nqb, p.by, p.bx, o0, o1, KV_SUB, p.Sq,
+    build_row(p.mask + bh * per_head, 1, p.nkb, p.by, p.bx, o0, o1, KV_SUB, p.Sq,
               sel_k + (size_t)gw * p.nQT_k, p.nQT_k, cnt_k + gw);
   } else if (gw < nk_rows + BH * p.nQT_q) {
     int r = gw - nk_rows;
     int bh = r / p.nQT_q, qt = r % p.nQT_q;
     int o0 = qt * Q_TILE, o1 = min(o0 + Q_TILE, p.Sq);
-    build_row(p.mask + (size_t)bh * p.nqb * p.nkb, p.nkb, p.bx, p.by, o0, o1, Q_SUB, p.Skv,
+    build_row(p.mask + bh * per_head, p.nkb, 1, p.bx, p.by, o0, o1, Q_SUB, p.Skv,
               sel_q + (size_t)r * p.nKT_q, p.nKT_q, cnt_q + r);
   }
 }
@@ -202,16 +215,23 @@ __global__ void k_build_sel(AttnParams p, int* __restrict__ sel_k, int* __restri
 cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const float* lse,
                               const float* sink, float* nlse2, float* delta, float* part, int B,
                               int Hq, int Sq, int Sq_pad, const int* seqlen_q, const int* cu_q,
-                              int total_q, cudaStream_t st) {
-  dim3 grid(Sq_pad / PREP_BLOCK_ROWS, B * Hq);
-  int nparts = B * (Sq_pad / PREP_BLOCK_ROWS);
-  if (bf16)
-    k_preprocess<true><<<grid, 256, 0, st>>>((const uint4*)O, (const uint4*)dO, lse, sink, nlse2,
-                                              delta, part, Hq, Sq, Sq_pad, nparts, seqlen_q, cu_q, total_q);
-  else
-    k_preprocess<false><<<grid, 256, 0, st>>>((const uint4*)O, (const uint4*)dO, lse, sink, nlse2,
-                                               delta, part, Hq, Sq, Sq_pad, nparts, seqlen_q, cu_q, total_q);
-  return cudaGetLastError();
+                              int total_q, bool overlap_prev, cudaStream_t st) {
+  const int nparts = B * (Sq_pad / PREP_BLOCK_ROWS);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(Sq_pad / PREP_BLOCK_ROWS, B * Hq);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_prev ? 1 : 0;
+  const uint4* o4 = (const uint4*)O;
+  const uint4* d4 = (const uint4*)dO;
+  return bf16 ? cudaLaunchKernelEx(&cfg, k_preprocess<true>, o4, d4, lse, sink, nlse2, delta, part,
+                                   Hq, Sq, Sq_pad, nparts, seqlen_q, cu_q, total_q)
+              : cudaLaunchKernelEx(&cfg, k_preprocess<false>, o4, d4, lse, sink, nlse2, delta,
+                                   part, Hq, Sq, Sq_pad, nparts, seqlen_q, cu_q, total_q);
 }
 
 cudaError_t launch_dsink_finalize(const float* part, int Hq, int nparts, float* dsink,
@@ -220,18 +240,14 @@ cudaError_t launch_dsink_finalize(const float* part, int Hq, int nparts, float* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_mask_transpose(const uint8_t* mask, uint8_t* maskT, int BH, int nqb, int nkb,
-                                  cudaStream_t st) {
-  dim3 grid((nkb + 31) / 32, (nqb + 31) / 32, BH < 65535 ? BH : 65535);
-  k_mask_transpose<<<grid, dim3(32, 8), 0, st>>>(mask, maskT, BH, nqb, nkb);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_build_sel(const AttnParams& p, int* sel_k, int* cnt_k, int* sel_q, int* cnt_q,
-                             cudaStream_t st) {
-  long long rows = (long long)p.B * p.Hq * ((long long)p.nKT_k + p.nQT_q);
-  int blocks = (int)((rows + 3) / 4);
-  k_build_sel<<<blocks, 128, 0, st>>>(p, sel_k, cnt_k, sel_q, cnt_q);
+cudaError_t launch_mask_tables(const AttnParams& p, uint8_t* maskT, int* sel_k, int* cnt_k,
+                               int* sel_q, int* cnt_q, cudaStream_t st) {
+  const long long BH = (long long)p.B * p.Hq;
+  const long long n_tr = BH * ((p.nkb + 31) / 32) * ((p.nqb + 31) / 32);
+  const long long rows = BH * ((long long)p.nKT_k + p.nQT_q);
+  const long long blocks = n_tr + (rows + 3) / 4;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  k_mask_tables<<<(unsigned)blocks, 128, 0, st>>>(p, maskT, (int)n_tr, sel_k, cnt_k, sel_q, cnt_q);
   return cudaGetLastError();
 }
 

@@ -20,6 +20,7 @@ struct DevStatus {
   unsigned int where;     // which wait gave up (kernel-specific tag)
   unsigned int block;     // blockIdx.x of the first CTA that gave up
   unsigned int next_unit;  // work counter of the persistent kernels (zeroed with the rest)
+  unsigned int kv_done;    // CTAs of the dK/dV grid that finished (the last one sums dSink)
 };
 
 struct WaitCtx {
