@@ -158,6 +158,16 @@ int test_no_loads() {
   return (e && e[0] == '1') ? 1 : 0;
 }
 
+// Test hook (MASKATTN_DKDV_SCHEDULE=tile|units): forces the dK/dV kernel's
+// form, so that the tests run both on any shape.
+int dkdv_schedule() {
+  const char* e = getenv("MASKATTN_DKDV_SCHEDULE");
+  if (!e) return 0;
+  if (strcmp(e, "tile") == 0) return 1;
+  if (strcmp(e, "units") == 0) return 2;
+  return 0;
+}
+
 unsigned long long wait_timeout_ns() {
   const char* e = getenv("MASKATTN_WAIT_TIMEOUT_NS");
   if (e && *e) {
@@ -204,6 +214,7 @@ AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const W
   p.status = reinterpret_cast<DevStatus*>(ws + L.status);
   p.timeout_ns = wait_timeout_ns();
   p.test_no_loads = test_no_loads();
+  p.kv_schedule = dkdv_schedule();
   p.compensated = (sh->flags & ATTN_FLAG_COMPENSATED) ? 1 : 0;
   if (sh->flags & ATTN_FLAG_SINGLE_PASS) {
     p.dq_part = reinterpret_cast<float*>(ws + L.dq_part);

@@ -35,7 +35,7 @@
 // 16 g .. 16 g + 15 of each dQ partial.
 #include <math.h>
 
-#include "tiles.cuh"
+#include "kv_softmax.cuh"
 
 namespace mab {
 
@@ -375,34 +375,11 @@ k_dkdvq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
       } else {
         vis = vis_key_row(p, b * p.Hq + c * p.group + hh, j, r * KV_SUB + 16 * g, Lq, Lk);
       }
-      const float4* l4 = reinterpret_cast<const float4*>(&s.nlse2[st][16 * g]);
       float lv[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 L = l4[q];
-        lv[4 * q] = L.x;
-        lv[4 * q + 1] = L.y;
-        lv[4 * q + 2] = L.z;
-        lv[4 * q + 3] = L.w;
-      }
+      load16_shared(&s.nlse2[st][16 * g], lv);
       tmem_wait_ld_regs(sv);
-      if (!full) {
-#pragma unroll
-        for (int cc = 0; cc < 16; ++cc) sv[cc] = ((vis >> cc) & 1u) ? sv[cc] : -INFINITY;
-      }
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       float pv[16];
-      uint32_t pk[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float2 x = ffma2(make_float2(sv[2 * q], sv[2 * q + 1]), sc2,
-                               make_float2(lv[2 * q], lv[2 * q + 1]));
-        pv[2 * q] = fast_exp2(x.x);
-        pv[2 * q + 1] = fast_exp2(x.y);
-        pk[q] = pack2<BF16>(pv[2 * q], pv[2 * q + 1]);
-      }
-      tmem_st8(lane_base + COL_S + 16 * g, pk);
-      tmem_wait_st();
+      kv_write_p<BF16, false>(lane_base + COL_S + 16 * g, sv, lv, full, vis, p.scale_log2, pv);
       warp_arrive(&s.bar_p_full);
 
       // ---- the previous step's dQ partial (its completion also frees the
@@ -413,16 +390,8 @@ k_dkdvq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
       }
 
       // ---- dS^T(n) = P^T(n) (dP^T(n) - Delta), to TMEM and shared memory
-      const float4* d4 = reinterpret_cast<const float4*>(&s.delta[st][16 * g]);
       float dl[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 D = d4[q];
-        dl[4 * q] = D.x;
-        dl[4 * q + 1] = D.y;
-        dl[4 * q + 2] = D.z;
-        dl[4 * q + 3] = D.w;
-      }
+      load16_shared(&s.delta[st][16 * g], dl);
       if (!mbar_wait(smem_u32(&s.bar_dp_full), n & 1, wc, TAG_DP_FULL)) {
         ok = false;
         break;
@@ -431,14 +400,8 @@ k_dkdvq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
       float dp[16];
       tmem_ld16(lane_base + COL_DP + 16 * g, dp);
       tmem_wait_ld_regs(dp);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float2 ds = fmul2(make_float2(pv[2 * q], pv[2 * q + 1]),
-                                fsub2(make_float2(dp[2 * q], dp[2 * q + 1]),
-                                      make_float2(dl[2 * q], dl[2 * q + 1])));
-        pk[q] = pack2<BF16>(ds.x, ds.y);
-      }
-      tmem_st8(lane_base + COL_DP + 16 * g, pk);
+      uint32_t pk[8];
+      kv_write_ds<BF16, false>(lane_base + COL_DP + 16 * g, pv, dp, dl, pk);
       // key row rloc, queries 16 g .. 16 g + 15: two 16-byte chunks of the
       // 128-byte row, 128B-swizzled (chunk index xor row % 8)
       uint8_t* row = s.dS + rloc * 128;
@@ -448,7 +411,6 @@ k_dkdvq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensor
           make_uint4(pk[4], pk[5], pk[6], pk[7]);
       // the dQ^T MMA reads the tile through the async proxy
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      tmem_wait_st();
       warp_arrive(&s.bar_ds_full);
       prev_r = r;
       prev_hh = hh;

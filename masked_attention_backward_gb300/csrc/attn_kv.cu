@@ -47,7 +47,7 @@
 // 32 sp .. 32 sp + 31 (key rows) and query columns 16 g .. 16 g + 15.
 #include <math.h>
 
-#include "tiles.cuh"
+#include "kv_softmax.cuh"
 
 namespace mab {
 
@@ -371,58 +371,16 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
         vis = vis_key_row(p, b * p.Hq + c * p.group + s.step_hh[st], j, r * KV_SUB + 16 * g, Lq,
                           Lk);
       }
-      const float4* l4 = reinterpret_cast<const float4*>(&s.nlse2[st][16 * g]);
       float lv[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 L = l4[q];
-        lv[4 * q] = L.x;
-        lv[4 * q + 1] = L.y;
-        lv[4 * q + 2] = L.z;
-        lv[4 * q + 3] = L.w;
-      }
+      load16_shared(&s.nlse2[st][16 * g], lv);
       tmem_wait_ld_regs(sv);
-      // an invisible logit becomes -inf, so its P is 0 (and so is its dS)
-      if (!full) {
-#pragma unroll
-        for (int cc = 0; cc < 16; ++cc) sv[cc] = ((vis >> cc) & 1u) ? sv[cc] : -INFINITY;
-      }
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       float pv[16];
-      uint32_t pk[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float2 x = ffma2(make_float2(sv[2 * q], sv[2 * q + 1]), sc2,
-                               make_float2(lv[2 * q], lv[2 * q + 1]));
-        pv[2 * q] = fast_exp2(x.x);
-        pv[2 * q + 1] = fast_exp2(x.y);
-        pk[q] = pack2<BF16>(pv[2 * q], pv[2 * q + 1]);
-      }
-      // over this warp's own S^T columns, which it has just loaded
-      tmem_st8(lane_base + colS, pk);
-      if constexpr (HILO) {
-        uint32_t pl[8];  // remainders P - high part
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float2 h = unpack2<BF16>(pk[q]);
-          pl[q] = pack2<BF16>(pv[2 * q] - h.x, pv[2 * q + 1] - h.y);
-        }
-        tmem_st8(lane_base + colS + 8, pl);
-      }
-      tmem_wait_st();
+      kv_write_p<BF16, HILO>(lane_base + colS, sv, lv, full, vis, p.scale_log2, pv);
       warp_arrive(&s.bar_p_full[bf]);
 
       // ---- dS^T(n) = P^T(n) (dP^T(n) - Delta)
-      const float4* d4 = reinterpret_cast<const float4*>(&s.delta[st][16 * g]);
       float dl[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 D = d4[q];
-        dl[4 * q] = D.x;
-        dl[4 * q + 1] = D.y;
-        dl[4 * q + 2] = D.z;
-        dl[4 * q + 3] = D.w;
-      }
+      load16_shared(&s.delta[st][16 * g], dl);
       if (!mbar_wait(smem_u32(&s.bar_dp_full[bf]), (n >> 1) & 1, wc, TAG_DP_FULL)) {
         ok = false;
         break;
@@ -431,28 +389,8 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
       float dp[16];
       tmem_ld16(lane_base + colS + 64, dp);
       tmem_wait_ld_regs(dp);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float2 ds = fmul2(make_float2(pv[2 * q], pv[2 * q + 1]),
-                                fsub2(make_float2(dp[2 * q], dp[2 * q + 1]),
-                                      make_float2(dl[2 * q], dl[2 * q + 1])));
-        pk[q] = pack2<BF16>(ds.x, ds.y);
-        if (HILO) {
-          dp[2 * q] = ds.x;
-          dp[2 * q + 1] = ds.y;
-        }
-      }
-      tmem_st8(lane_base + colS + 64, pk);
-      if constexpr (HILO) {
-        uint32_t pl[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float2 h = unpack2<BF16>(pk[q]);
-          pl[q] = pack2<BF16>(dp[2 * q] - h.x, dp[2 * q + 1] - h.y);
-        }
-        tmem_st8(lane_base + colS + 64 + 8, pl);
-      }
-      tmem_wait_st();
+      uint32_t pk[8];
+      kv_write_ds<BF16, HILO>(lane_base + colS + 64, pv, dp, dl, pk);
       warp_arrive(&s.bar_ds_full[bf]);
     }
     // ---------------------------------------------------------- epilogue
@@ -514,9 +452,29 @@ k_dkdv(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorM
   }
 }
 
+// Whether the persistent form (attn_kv_units.cu) runs the dK/dV walk: for the
+// BHSD layout when there are at least two units per SM and the walks are
+// short -- block masks, or closed-form masks whose key tiles average at most
+// 64 steps at the full lengths -- where a CTA per unit would spend much of
+// its time starting and storing.  On long walks the per-tile grid is faster.
+static bool use_units(const AttnParams& p) {
+  if (p.cu_q) return false;
+  if (p.kv_schedule != 0) return p.kv_schedule == 2;
+  const long long units = (long long)p.nKT_k * p.B * p.Hkv;
+  if (units < 2LL * (p.num_sms > 0 ? p.num_sms : 1)) return false;
+  if (p.mask_kind == MK_BLOCK) return true;
+  long long steps = 0;
+  for (int t = 0; t < p.nKT_k; ++t) {
+    int lo;
+    steps += kv_tile_range_full(p.mask_kind, p.window, p.Sq, p.Skv, t, &lo);
+  }
+  return steps * p.group <= 64LL * p.nKT_k;
+}
+
 cudaError_t launch_dkdv(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                         const CUtensorMap& tdO, const CUtensorMap& tK, const CUtensorMap& tV,
                         void* dk, void* dv, cudaStream_t st) {
+  if (use_units(p)) return launch_dkdv_units(bf16, p, tQ, tdO, tK, tV, dk, dv, st);
   using Kern = decltype(&k_dkdv<true, false, false>);
   static const Kern table[2][2][2] = {
       {{k_dkdv<false, false, false>, k_dkdv<false, false, true>},

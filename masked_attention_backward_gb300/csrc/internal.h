@@ -64,6 +64,7 @@ struct AttnParams {
   const int* seqlen_q; // [B] valid query rows per batch, or nullptr (= Sq)
   const int* seqlen_k; // [B] valid keys per batch, or nullptr (= Skv)
   int num_sms;         // SMs of the device (CTAs resident at once in one-CTA-per-SM grids)
+  int kv_schedule;     // test hook: 0 = chosen by the walk lengths, 1 = per tile, 2 = persistent
   // Packed layout: sequence b holds tokens [cu_q[b], cu_q[b + 1]) of the
   // token-major tensors q, o, dO, dq [total_q, Hq, 128] (lse [Hq, total_q])
   // and [cu_k[b], cu_k[b + 1]) of k, v, dk, dv [total_k, Hkv, 128]; Sq and
@@ -166,6 +167,9 @@ cudaError_t launch_mask_tables(const AttnParams& p, uint8_t* maskT, int* sel_k, 
 cudaError_t launch_dkdv(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                         const CUtensorMap& tdO, const CUtensorMap& tK, const CUtensorMap& tV,
                         void* dk, void* dv, cudaStream_t st);
+cudaError_t launch_dkdv_units(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
+                              const CUtensorMap& tdO, const CUtensorMap& tK,
+                              const CUtensorMap& tV, void* dk, void* dv, cudaStream_t st);
 cudaError_t launch_dq(bool bf16, const AttnParams& p, const CUtensorMap& tQ, const CUtensorMap& tdO,
                       const CUtensorMap& tK, const CUtensorMap& tV, void* dq, cudaStream_t st);
 cudaError_t launch_fwd(bool bf16, const AttnParams& p, const CUtensorMap& tQ,

@@ -21,6 +21,7 @@ struct DevStatus {
   unsigned int block;     // blockIdx.x of the first CTA that gave up
   unsigned int next_unit;  // work counter of the persistent kernels (zeroed with the rest)
   unsigned int kv_done;    // CTAs of the dK/dV grid that finished (the last one sums dSink)
+  unsigned int next_unit_kv;  // work counter of the persistent dK/dV kernel
 };
 
 struct WaitCtx {
@@ -87,6 +88,28 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
         }
         return false;
       }
+    }
+  }
+}
+
+// mbar_wait for waits expected to be long, by warps off the critical path:
+// polls every `sleep_ns` nanoseconds, leaving the issue slots in between to
+// the other warps of the SM sub-partition.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                                unsigned int tag, unsigned int sleep_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(sleep_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*w.abort_flag) return false;
+    if (globaltimer_ns() - t0 > w.timeout_ns) {
+      *w.abort_flag = 1;
+      if (atomicCAS(&w.status->code, 0u, 5u /*ATTN_ERR_TIMEOUT*/) == 0u) {
+        w.status->where = tag;
+        w.status->block = blockIdx.x;
+      }
+      return false;
     }
   }
 }

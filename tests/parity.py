@@ -185,7 +185,7 @@ def ws_layout(wl: Workload, single_pass: bool = False) -> dict:
     Sq_pad = cdiv(wl.Sq, PREP_ROWS) * PREP_ROWS
     BH = wl.B * wl.Hq
     L = {"status": 0}
-    off = _a256(20)  # the status word
+    off = _a256(24)  # the status word
     L["nlse2"] = off; off = _a256(off + BH * Sq_pad * 4)
     L["delta"] = off; off = _a256(off + BH * Sq_pad * 4)
     L["dsink_part"] = off; off = _a256(off + wl.Hq * wl.B * (Sq_pad // PREP_BLOCK_ROWS) * 4)
