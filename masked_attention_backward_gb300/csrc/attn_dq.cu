@@ -477,16 +477,12 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         const int bf = m & 1, st = rg.st;
         // s_full implies the stage's loads landed; waiting on kv_full as well
         // makes the step's tile index (written by the producer) visible
-        if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (m >> 1) & 1, wc, TAG_S_FULL) ||
-            !mbar_wait(smem_u32(&s.bar_kv_full[st]), rg.ph, wc, TAG_KV_FULL)) {
+        // the step's tile index (and, block masks, the mask bytes its
+        // visibility needs) are read while S and dP are still being computed
+        if (!mbar_wait(smem_u32(&s.bar_kv_full[st]), rg.ph, wc, TAG_KV_FULL)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t col = COL_BUF + bf * 128 + 32 * g;
-        float sv[32], dp[32];
-        tmem_ld32(lane_base + col, sv);
-        tmem_ld32(lane_base + col + 64, dp);
         const int t = s.step_t[st];
         // warp-uniform: the whole 128 x 64 sub-tile is visible
         const bool full = t >= flo && t <= fhi;
@@ -500,6 +496,15 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         } else {
           vis = vis_query_row(p, un.bh, i, t * Q_SUB + 32 * g, p.Sq, VARLEN ? Lk : p.Skv);
         }
+        if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (m >> 1) & 1, wc, TAG_S_FULL)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t col = COL_BUF + bf * 128 + 32 * g;
+        float sv[32], dp[32];
+        tmem_ld32(lane_base + col, sv);
+        tmem_ld32(lane_base + col + 64, dp);
         tmem_wait_ld_regs(sv);
 #pragma unroll
         for (int c = 0; c < 32; ++c) asm volatile("" : "+f"(dp[c]));

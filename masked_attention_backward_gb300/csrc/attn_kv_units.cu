@@ -415,14 +415,12 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
         const uint32_t colS = COL_BUF + 128 * bf + 16 * g;
         // s_full implies the stage's loads landed; waiting on q_full as well
         // makes the bulk-copied rows and the step's coordinates visible
-        if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (gn >> 1) & 1, wc, TAG_S_FULL) ||
-            !mbar_wait(smem_u32(&s.bar_q_full[st]), (gn / NST) & 1, wc, TAG_Q_FULL)) {
+        // the step's coordinates (and, block masks, the mask bytes its
+        // visibility needs) are read while S^T is still being computed
+        if (!mbar_wait(smem_u32(&s.bar_q_full[st]), (gn / NST) & 1, wc, TAG_Q_FULL)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        float sv[16];
-        tmem_ld16(lane_base + colS, sv);
         const int r = s.step_r[st];
         const bool full = r >= flo && r <= fhi;
         uint32_t vis;
@@ -438,6 +436,13 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
         }
         float lv[16];
         load16_shared(&s.nlse2[st][16 * g], lv);
+        if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (gn >> 1) & 1, wc, TAG_S_FULL)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sv[16];
+        tmem_ld16(lane_base + colS, sv);
         tmem_wait_ld_regs(sv);
         float pv[16];
         kv_write_p<BF16, HILO>(lane_base + colS, sv, lv, full, vis, p.scale_log2, pv);
