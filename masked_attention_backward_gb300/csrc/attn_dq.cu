@@ -433,6 +433,12 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       if (u < 0) break;
       DqUnit un{};
       un.template init<VARLEN>(p, u);
+      // this row's statistics, loaded now so that their latency passes while
+      // the warp copies Q / dO and stores the previous unit
+      const int i = un.q0 + rloc;
+      const size_t srow = (size_t)un.bh * p.Sq_pad + i;
+      const float nlse2_i = p.nlse2[srow];  // -lse log2(e)
+      const float delta_i = p.delta[srow];
       // Q and dO rows of the unit into TMEM as 16-bit pairs (element 2c in
       // the low half of column c): this warp copies d columns
       // 64 g .. 64 g + 63 of its rows.  Every S / dP MMA of the previous unit
@@ -464,10 +470,6 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&s.bar_unit_free));
 
-      const int i = un.q0 + rloc;
-      const size_t srow = (size_t)un.bh * p.Sq_pad + i;
-      const float nlse2_i = p.nlse2[srow];  // -lse log2(e)
-      const float delta_i = p.delta[srow];
       int flo, fhi;  // key sub-tiles that are entirely visible
       // keys past the batch's length are masked here; rows past its length
       // need no mask: their -lse log2 e is -inf, so their P and dS are 0
