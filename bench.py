@@ -42,7 +42,8 @@ MASK_NAMES = {0: "none", 1: "causal", 2: "causal+sliding window", 3: "block"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # Files whose content decides the dK/dV and dQ kernels' DRAM traffic.
 KERNEL_SOURCES = {
-    "k_dkdv": ["csrc/attn_kv.cu", "csrc/tiles.cuh", "csrc/ptx.cuh", "csrc/internal.h"],
+    "k_dkdv": ["csrc/attn_kv.cu", "csrc/kv_softmax.cuh", "csrc/tiles.cuh", "csrc/ptx.cuh",
+               "csrc/internal.h"],
     "k_dq": ["csrc/attn_dq.cu", "csrc/tiles.cuh", "csrc/ptx.cuh", "csrc/internal.h"],
 }
 
