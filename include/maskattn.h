@@ -42,12 +42,14 @@
  * an error nothing is enqueued and the outputs are left untouched.  Device
  * waits inside the kernels are bounded: a wait that runs out records
  * ATTN_ERR_TIMEOUT in the workspace status word, which attn_get_device_status
- * reads back.  The limit is 2 s per wait, or MASKATTN_WAIT_TIMEOUT_NS
- * nanoseconds from the environment at the time of the call.  Test hook:
- * with MASKATTN_TEST_NO_LOADS=1 in the environment at the time of a call, the
- * kernels' loader warps issue nothing, so the call's waits run out and it
- * ends with ATTN_ERR_TIMEOUT (outputs undefined); it exists to exercise this
- * path and is off unless set.
+ * reads back; the outputs of such a call are undefined.  The limit is 2 s per
+ * wait, or MASKATTN_WAIT_TIMEOUT_NS nanoseconds from the environment at the
+ * time of the call.  Test hooks, off unless set in the environment at the time
+ * of a call: MASKATTN_TEST_NO_LOADS=1 makes the kernels' loader warps issue
+ * nothing, so the call's waits run out and it ends with ATTN_ERR_TIMEOUT;
+ * MASKATTN_DKDV_SCHEDULE=tile or =units forces the per-tile or the persistent
+ * form of the dK/dV kernel (otherwise chosen by the walk lengths; the results
+ * are the same bit for bit).
  */
 #ifndef MASKATTN_H_
 #define MASKATTN_H_
