@@ -186,98 +186,223 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && !p.test_no_loads) {
-      tma_prefetch_desc(&tQ);
-      tma_prefetch_desc(&tdO);
-      tma_prefetch_desc(&tK);
-      tma_prefetch_desc(&tV);
-      bool ok = true;
-      int m = 0;  // step counter across units
-      int q_loaded = -1;  // last unit whose Q / dO tiles were loaded
-      Ring rg;
-      const uint32_t qbar = smem_u32(&s.bar_q_full);
-      for (int j = 0; ok; ++j) {
-        // the Q / dO tiles and the unit slot are free once every other warp
-        // has taken the previous unit (the softmax warps: copied its Q / dO
-        // into TMEM and stored the epilogue before it, staged in the Q tile)
-        if (j >= 1 && !mbar_wait(smem_u32(&s.bar_unit_free), (j - 1) & 1, wc, TAG_UNIT_FREE)) {
-          ok = false;
-          break;
-        }
-        int u = j == 0 ? (int)blockIdx.x : (int)(gridDim.x + atomicAdd(&p.status->next_unit, 1u));
-        if (u >= U) u = -1;
-        s.unit = u;  // published by the arrive on q_full
-        if (u < 0) {
-          mbar_arrive(qbar);
-          break;
-        }
-        DqUnit un{};
-        un.template init<VARLEN>(p, u);
-        if (un.walk.cnt == 0) {
-          // nothing to contract: the unit's rows only get zeros, so its
-          // Q / dO tiles are not loaded
-          mbar_arrive(qbar);
-        } else {
-          // packed layout (always with per-batch lengths): token coordinates;
-          // BHSD: (row, head)
-          const RowAddr qa = VARLEN ? row_q(p, un.bh / p.Hq, un.h, un.q0)
-                                    : RowAddr{un.q0, un.bh, 0, HEAD_DIM};
-          mbar_arrive_expect_tx(qbar, 4 * Q_TILE * 128);
-          tma_load_3d(smem_u32(s.Q), &tQ, 0, qa.c1, qa.c2, qbar);
-          tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, qa.c1, qa.c2, qbar);
-          tma_load_3d(smem_u32(s.dO), &tdO, 0, qa.c1, qa.c2, qbar);
-          tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, qa.c1, qa.c2, qbar);
-          q_loaded = j;
-        }
-        for (int n = 0; n < un.walk.cnt; ++n, ++m, rg.next()) {
-          const int st = rg.st;
-          const int t = un.walk.tile(n);
-          // aligned block masks: the mask byte of each softmax warp's 32-query
-          // x 32-key region, loaded before the wait below (which hides the
-          // latency; indices clamped into the mask, ranges applied after)
-          uint32_t mv[8];
-          if (blk_regions) {
-            const uint8_t* mb = p.mask + (size_t)un.bh * p.nqb * p.nkb;
-#pragma unroll
-            for (int sp2 = 0; sp2 < 4; ++sp2) {
-              const int qb = min((un.q0 + 32 * sp2) / p.bx, p.nqb - 1);
-#pragma unroll
-              for (int g2 = 0; g2 < 2; ++g2) {
-                const int kb = min((t * Q_SUB + 32 * g2) / p.by, p.nkb - 1);
-                mv[2 * sp2 + g2] = mb[(size_t)qb * p.nkb + kb];
-              }
-            }
-          }
-          if (m >= STAGES &&
-              !mbar_wait(smem_u32(&s.bar_kv_empty[st]), rg.ph ^ 1u, wc,
-                         TAG_KV_EMPTY)) {
+    // Without per-batch lengths the whole warp runs the walk and lane 0
+    // claims units and issues the copies: every 32 steps the lanes look up
+    // the next 32 steps at once (key sub-tile from the select table, aligned
+    // block masks' region word from the mask), so that no step waits for a
+    // chain of global loads of its own (random 30 % blocks: k_dq 0.411 ->
+    // 0.302 ms).  The per-batch-length instance, whose registers are at their
+    // limit, keeps lane 0 walking alone (the warp-wide form measured 7 %
+    // slower there).
+    if constexpr (VARLEN) {
+      if (lane == 0 && !p.test_no_loads) {
+        tma_prefetch_desc(&tQ);
+        tma_prefetch_desc(&tdO);
+        tma_prefetch_desc(&tK);
+        tma_prefetch_desc(&tV);
+        bool ok = true;
+        int m = 0;  // step counter across units
+        int q_loaded = -1;  // last unit whose Q / dO tiles were loaded
+        Ring rg;
+        const uint32_t qbar = smem_u32(&s.bar_q_full);
+        for (int j = 0; ok; ++j) {
+          // the Q / dO tiles and the unit slot are free once every other warp
+          // has taken the previous unit (the softmax warps: copied its Q / dO
+          // into TMEM and stored the epilogue before it, staged in the Q tile)
+          if (j >= 1 && !mbar_wait(smem_u32(&s.bar_unit_free), (j - 1) & 1, wc, TAG_UNIT_FREE)) {
             ok = false;
             break;
           }
-          s.step_t[st] = t;  // published by the arrive below together with the loads
-          if (blk_regions) {
-            uint32_t w = 0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              if (mv[e] && un.q0 + 32 * (e >> 1) < p.Sq && t * Q_SUB + 32 * (e & 1) < p.Skv)
-                w |= 1u << e;
-            s.step_vis[st] = w;
+          int u = j == 0 ? (int)blockIdx.x : (int)(gridDim.x + atomicAdd(&p.status->next_unit, 1u));
+          if (u >= U) u = -1;
+          s.unit = u;  // published by the arrive on q_full
+          if (u < 0) {
+            mbar_arrive(qbar);
+            break;
           }
-          const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
-          const RowAddr ka = VARLEN ? row_k(p, un.kvh / p.Hkv, un.kvh % p.Hkv, t * Q_SUB)
-                                    : RowAddr{t * Q_SUB, un.kvh, 0, HEAD_DIM};
-          mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
-          tma_load_3d(smem_u32(s.K[st]), &tK, 0, ka.c1, ka.c2, fb);
-          tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, ka.c1, ka.c2, fb);
-          tma_load_3d(smem_u32(s.V[st]), &tV, 0, ka.c1, ka.c2, fb);
-          tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, ka.c1, ka.c2, fb);
+          DqUnit un{};
+          un.template init<VARLEN>(p, u);
+          if (un.walk.cnt == 0) {
+            // nothing to contract: the unit's rows only get zeros, so its
+            // Q / dO tiles are not loaded
+            mbar_arrive(qbar);
+          } else {
+            // packed layout (always with per-batch lengths): token coordinates;
+            // BHSD: (row, head)
+            const RowAddr qa = VARLEN ? row_q(p, un.bh / p.Hq, un.h, un.q0)
+                                      : RowAddr{un.q0, un.bh, 0, HEAD_DIM};
+            mbar_arrive_expect_tx(qbar, 4 * Q_TILE * 128);
+            tma_load_3d(smem_u32(s.Q), &tQ, 0, qa.c1, qa.c2, qbar);
+            tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, qa.c1, qa.c2, qbar);
+            tma_load_3d(smem_u32(s.dO), &tdO, 0, qa.c1, qa.c2, qbar);
+            tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, qa.c1, qa.c2, qbar);
+            q_loaded = j;
+          }
+          for (int n = 0; n < un.walk.cnt; ++n, ++m, rg.next()) {
+            const int st = rg.st;
+            const int t = un.walk.tile(n);
+            // aligned block masks: the mask byte of each softmax warp's 32-query
+            // x 32-key region, loaded before the wait below (which hides the
+            // latency; indices clamped into the mask, ranges applied after)
+            uint32_t mv[8];
+            if (blk_regions) {
+              const uint8_t* mb = p.mask + (size_t)un.bh * p.nqb * p.nkb;
+  #pragma unroll
+              for (int sp2 = 0; sp2 < 4; ++sp2) {
+                const int qb = min((un.q0 + 32 * sp2) / p.bx, p.nqb - 1);
+  #pragma unroll
+                for (int g2 = 0; g2 < 2; ++g2) {
+                  const int kb = min((t * Q_SUB + 32 * g2) / p.by, p.nkb - 1);
+                  mv[2 * sp2 + g2] = mb[(size_t)qb * p.nkb + kb];
+                }
+              }
+            }
+            if (m >= STAGES &&
+                !mbar_wait(smem_u32(&s.bar_kv_empty[st]), rg.ph ^ 1u, wc,
+                           TAG_KV_EMPTY)) {
+              ok = false;
+              break;
+            }
+            s.step_t[st] = t;  // published by the arrive below together with the loads
+            if (blk_regions) {
+              uint32_t w = 0;
+  #pragma unroll
+              for (int e = 0; e < 8; ++e)
+                if (mv[e] && un.q0 + 32 * (e >> 1) < p.Sq && t * Q_SUB + 32 * (e & 1) < p.Skv)
+                  w |= 1u << e;
+              s.step_vis[st] = w;
+            }
+            const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
+            const RowAddr ka = VARLEN ? row_k(p, un.kvh / p.Hkv, un.kvh % p.Hkv, t * Q_SUB)
+                                      : RowAddr{t * Q_SUB, un.kvh, 0, HEAD_DIM};
+            mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
+            tma_load_3d(smem_u32(s.K[st]), &tK, 0, ka.c1, ka.c2, fb);
+            tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, ka.c1, ka.c2, fb);
+            tma_load_3d(smem_u32(s.V[st]), &tV, 0, ka.c1, ka.c2, fb);
+            tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, ka.c1, ka.c2, fb);
+          }
+        }
+        if (!ok) {
+          // the CTA gave up: let the copies still in flight land before it exits
+          if (q_loaded >= 0) mbar_drain(qbar, q_loaded & 1, wc.timeout_ns);
+          for (int k = m > STAGES ? m - STAGES : 0; k < m; ++k)
+            mbar_drain(smem_u32(&s.bar_kv_full[k % STAGES]), (k / STAGES) & 1, wc.timeout_ns);
         }
       }
-      if (!ok) {
-        // the CTA gave up: let the copies still in flight land before it exits
-        if (q_loaded >= 0) mbar_drain(qbar, q_loaded & 1, wc.timeout_ns);
-        for (int k = m > STAGES ? m - STAGES : 0; k < m; ++k)
-          mbar_drain(smem_u32(&s.bar_kv_full[k % STAGES]), (k / STAGES) & 1, wc.timeout_ns);
+    } else {
+      if (!p.test_no_loads) {
+        if (lane == 0) {
+          tma_prefetch_desc(&tQ);
+          tma_prefetch_desc(&tdO);
+          tma_prefetch_desc(&tK);
+          tma_prefetch_desc(&tV);
+        }
+        // lane 0 waits; the rest of the warp waits for its answer
+        auto wait0 = [&](uint32_t bar, uint32_t parity, unsigned int tag) -> bool {
+          bool r = true;
+          if (lane == 0) r = mbar_wait(bar, parity, wc, tag);
+          return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+        };
+        bool ok = true;
+        int m = 0;  // step counter across units
+        int q_loaded = -1;  // last unit whose Q / dO tiles were loaded
+        Ring rg;
+        const uint32_t qbar = smem_u32(&s.bar_q_full);
+        for (int j = 0; ok; ++j) {
+          // the Q / dO tiles and the unit slot are free once every other warp
+          // has taken the previous unit (the softmax warps: copied its Q / dO
+          // into TMEM and stored the epilogue before it, staged in the Q tile)
+          if (j >= 1 && !wait0(smem_u32(&s.bar_unit_free), (j - 1) & 1, TAG_UNIT_FREE)) {
+            ok = false;
+            break;
+          }
+          int u = 0;
+          if (lane == 0) {
+            u = j == 0 ? (int)blockIdx.x : (int)(gridDim.x + atomicAdd(&p.status->next_unit, 1u));
+            if (u >= U) u = -1;
+          }
+          u = __shfl_sync(0xffffffffu, u, 0);
+          DqUnit un{};
+          if (u >= 0) un.template init<VARLEN>(p, u);
+          if (lane == 0) {
+            s.unit = u;  // published by the arrive on q_full
+            if (u < 0 || un.walk.cnt == 0) {
+              // nothing to contract: the unit's rows only
+              // get zeros, so its Q / dO tiles are not loaded
+              mbar_arrive(qbar);
+            } else {
+              // packed layout (always with per-batch lengths): token coordinates;
+              // BHSD: (row, head)
+              const RowAddr qa = VARLEN ? row_q(p, un.bh / p.Hq, un.h, un.q0)
+                                        : RowAddr{un.q0, un.bh, 0, HEAD_DIM};
+              mbar_arrive_expect_tx(qbar, 4 * Q_TILE * 128);
+              tma_load_3d(smem_u32(s.Q), &tQ, 0, qa.c1, qa.c2, qbar);
+              tma_load_3d(smem_u32(s.Q + Q_TILE * 128), &tQ, 64, qa.c1, qa.c2, qbar);
+              tma_load_3d(smem_u32(s.dO), &tdO, 0, qa.c1, qa.c2, qbar);
+              tma_load_3d(smem_u32(s.dO + Q_TILE * 128), &tdO, 64, qa.c1, qa.c2, qbar);
+              q_loaded = j;
+            }
+          }
+          if (u < 0) break;
+          for (int n0 = 0; ok && n0 < un.walk.cnt; n0 += 32) {
+            // lane l: step n0 + l
+            int t = 0;
+            uint32_t w = 0;
+            if (n0 + lane < un.walk.cnt) {
+              t = un.walk.tile(n0 + lane);
+              if (blk_regions) {
+                // the mask byte of each softmax warp's 32-query x 32-key region
+                // (indices clamped into the mask, ranges applied after)
+                const uint8_t* mb = p.mask + (size_t)un.bh * p.nqb * p.nkb;
+                uint32_t mv[8];
+    #pragma unroll
+                for (int sp2 = 0; sp2 < 4; ++sp2) {
+                  const int qb = min((un.q0 + 32 * sp2) / p.bx, p.nqb - 1);
+    #pragma unroll
+                  for (int g2 = 0; g2 < 2; ++g2) {
+                    const int kb = min((t * Q_SUB + 32 * g2) / p.by, p.nkb - 1);
+                    mv[2 * sp2 + g2] = mb[(size_t)qb * p.nkb + kb];
+                  }
+                }
+    #pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  if (mv[e] && un.q0 + 32 * (e >> 1) < p.Sq && t * Q_SUB + 32 * (e & 1) < p.Skv)
+                    w |= 1u << e;
+              }
+            }
+            const int cnt = min(32, un.walk.cnt - n0);
+            for (int k = 0; k < cnt; ++k, ++m, rg.next()) {
+              const int st = rg.st;
+              const int tk = __shfl_sync(0xffffffffu, t, k);
+              const uint32_t wk = __shfl_sync(0xffffffffu, w, k);
+              if (m >= STAGES && !wait0(smem_u32(&s.bar_kv_empty[st]), rg.ph ^ 1u, TAG_KV_EMPTY)) {
+                ok = false;
+                break;
+              }
+              if (lane == 0) {
+                s.step_t[st] = tk;  // published by the arrive below together with the loads
+                s.step_vis[st] = wk;
+                {
+                  const uint32_t fb = smem_u32(&s.bar_kv_full[st]);
+                  const RowAddr ka = VARLEN ? row_k(p, un.kvh / p.Hkv, un.kvh % p.Hkv, tk * Q_SUB)
+                                            : RowAddr{tk * Q_SUB, un.kvh, 0, HEAD_DIM};
+                  mbar_arrive_expect_tx(fb, 4 * Q_SUB * 128);
+                  tma_load_3d(smem_u32(s.K[st]), &tK, 0, ka.c1, ka.c2, fb);
+                  tma_load_3d(smem_u32(s.K[st] + Q_SUB * 128), &tK, 64, ka.c1, ka.c2, fb);
+                  tma_load_3d(smem_u32(s.V[st]), &tV, 0, ka.c1, ka.c2, fb);
+                  tma_load_3d(smem_u32(s.V[st] + Q_SUB * 128), &tV, 64, ka.c1, ka.c2, fb);
+                }
+              }
+              __syncwarp();
+            }
+          }
+        }
+        if (!ok && lane == 0) {
+          // the CTA gave up: let the copies still in flight land before it exits
+          if (q_loaded >= 0) mbar_drain(qbar, q_loaded & 1, wc.timeout_ns);
+          for (int k = m > STAGES ? m - STAGES : 0; k < m; ++k)
+            mbar_drain(smem_u32(&s.bar_kv_full[k % STAGES]), (k / STAGES) & 1, wc.timeout_ns);
+        }
       }
     }
   } else if (warp >= 1 && warp < SM_WARP0) {

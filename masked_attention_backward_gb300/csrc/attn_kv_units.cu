@@ -190,67 +190,88 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs the walk; lane 0 claims units and issues the copies.
+    // Every 32 steps the lanes look up the next 32 steps at once (query head,
+    // sub-tile from the select table, aligned block masks' region word from
+    // the transposed mask), so that no step waits for a chain of global
+    // loads of its own.
     if (lane == 0) {
       tma_prefetch_desc(&tQ);
       tma_prefetch_desc(&tdO);
       tma_prefetch_desc(&tK);
       tma_prefetch_desc(&tV);
-      const uint32_t kvbar = smem_u32(&s.bar_kv_full);
-      bool ok = true;
-      int gn = 0;               // steps issued, across units
-      int up = 0;               // units with steps so far
-      bool kv_pending = false;  // a K / V load was issued (the last one: phase up - 1)
-      for (int j = 0; ok; ++j) {
-        const int slot = j % USLOTS;
-        if (j >= USLOTS && !mbar_wait(smem_u32(&s.bar_unit_empty[slot]),
-                                      ((j / USLOTS) - 1) & 1, wc, TAG_UNIT_EMPTY)) {
-          ok = false;
-          break;
-        }
-        int u = j == 0 ? (int)blockIdx.x
-                       : (int)(gridDim.x + atomicAdd(&p.status->next_unit_kv, 1u));
+    }
+    const uint32_t kvbar = smem_u32(&s.bar_kv_full);
+    // lane 0 waits; the rest of the warp waits for its answer
+    auto wait0 = [&](uint32_t bar, uint32_t parity, unsigned int tag) -> bool {
+      bool r = true;
+      if (lane == 0) r = mbar_wait(bar, parity, wc, tag);
+      return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+    };
+    bool ok = true;
+    int gn = 0;               // steps issued, across units
+    int up = 0;               // units with steps so far
+    bool kv_pending = false;  // a K / V load was issued (the last one: phase up - 1)
+    for (int j = 0; ok; ++j) {
+      const int slot = j % USLOTS;
+      if (j >= USLOTS &&
+          !wait0(smem_u32(&s.bar_unit_empty[slot]), ((j / USLOTS) - 1) & 1, TAG_UNIT_EMPTY)) {
+        ok = false;
+        break;
+      }
+      int u = 0;
+      if (lane == 0) {
+        u = j == 0 ? (int)blockIdx.x : (int)(gridDim.x + atomicAdd(&p.status->next_unit_kv, 1u));
         if (u >= U) u = -1;
         s.unit[slot] = u;  // published by the arrive
         mbar_arrive(smem_u32(&s.bar_unit_full[slot]));
-        if (u < 0) break;
-        KvUnit un;
-        un.init(p, u);
-        // a key tile without any step only gets zeros: K and V are not loaded
-        if (un.N == 0) continue;
-        if (up >= 1) {
-          // bring the tile into L2 while the current unit's last MMAs run, and
-          // load it once they no longer read K and V
+      }
+      u = __shfl_sync(0xffffffffu, u, 0);
+      if (u < 0) break;
+      KvUnit un;
+      un.init(p, u);
+      // a key tile without any step only gets zeros: K and V are not loaded
+      if (un.N == 0) continue;
+      if (up >= 1) {
+        // bring the tile into L2 while the current unit's last MMAs run, and
+        // load it once they no longer read K and V
+        if (lane == 0) {
           tma_prefetch_l2_3d(&tK, 0, un.k0, un.bc);
           tma_prefetch_l2_3d(&tK, 64, un.k0, un.bc);
           tma_prefetch_l2_3d(&tV, 0, un.k0, un.bc);
           tma_prefetch_l2_3d(&tV, 64, un.k0, un.bc);
-          if (!mbar_wait(smem_u32(&s.bar_k_free), (up - 1) & 1, wc, TAG_KV_FREE) ||
-              !mbar_wait(smem_u32(&s.bar_v_free), (up - 1) & 1, wc, TAG_KV_FREE)) {
-            ok = false;
-            break;
-          }
         }
-        if (!p.test_no_loads) {
+        if (!wait0(smem_u32(&s.bar_k_free), (up - 1) & 1, TAG_KV_FREE) ||
+            !wait0(smem_u32(&s.bar_v_free), (up - 1) & 1, TAG_KV_FREE)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!p.test_no_loads) {
+        if (lane == 0) {
           mbar_arrive_expect_tx(kvbar, 4 * KV_TILE * 128);
           tma_load_3d(smem_u32(s.K), &tK, 0, un.k0, un.bc, kvbar);
           tma_load_3d(smem_u32(s.K + KV_TILE * 128), &tK, 64, un.k0, un.bc, kvbar);
           tma_load_3d(smem_u32(s.V), &tV, 0, un.k0, un.bc, kvbar);
           tma_load_3d(smem_u32(s.V + KV_TILE * 128), &tV, 64, un.k0, un.bc, kvbar);
-          kv_pending = true;
         }
-        ++up;
-        KVCursor cur;
-        cur.start(p, un.walk);
-        for (int n = 0; n < un.N; ++n, ++gn) {
-          const int st = gn % NST;
-          int r, hh;
-          kv_step(p, un.walk, cur, &hh, &r);
-          const int bh = un.b * p.Hq + un.c * p.group + hh;
-          // aligned block masks: the mask byte of each softmax warp's region,
-          // loaded before the wait below (indices clamped, ranges applied after)
-          uint32_t mv[16];
+        kv_pending = true;
+      }
+      ++up;
+      for (int n0 = 0; ok && n0 < un.N; n0 += 32) {
+        // lane l: step n0 + l (head-major over the group's query heads)
+        int hh = 0, r = 0;
+        uint32_t w = 0;
+        if (n0 + lane < un.N) {
+          int idx = n0 + lane;
+          for (int c; hh < p.group - 1 && idx >= (c = un.walk.count(p, hh)); ++hh) idx -= c;
+          r = un.walk.tile(p, hh, idx);
           if (blk_regions) {
+            // the mask byte of each softmax warp's 32-key x 16-query region
+            // (indices clamped into the mask, ranges applied after)
+            const int bh = un.b * p.Hq + un.c * p.group + hh;
             const uint8_t* mt = p.maskT + (size_t)bh * p.nkb * p.nqb;
+            uint32_t mv[16];
 #pragma unroll
             for (int sp2 = 0; sp2 < 4; ++sp2) {
               const int kb = min((un.k0 + 32 * sp2) / p.by, p.nkb - 1);
@@ -260,40 +281,49 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
                 mv[4 * sp2 + g2] = mt[(size_t)kb * p.nqb + qb];
               }
             }
-          }
-          if (gn >= NST &&
-              !mbar_wait(smem_u32(&s.bar_q_empty[st]), ((gn / NST) - 1) & 1, wc, TAG_Q_EMPTY)) {
-            ok = false;
-            break;
-          }
-          s.step_r[st] = r;  // published with the loads by the arrive below
-          s.step_hh[st] = hh;
-          if (blk_regions) {
-            uint32_t w = 0;
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               if (mv[e] && un.k0 + 32 * (e >> 2) < p.Skv && r * KV_SUB + 16 * (e & 3) < p.Sq)
                 w |= 1u << e;
-            s.step_vis[st] = w;
           }
-          if (p.test_no_loads) continue;
-          const uint32_t fb = smem_u32(&s.bar_q_full[st]);
-          mbar_arrive_expect_tx(fb, 4 * KV_SUB * 128 + 2 * KV_SUB * 4);
-          tma_load_3d(smem_u32(s.Q[st]), &tQ, 0, r * KV_SUB, bh, fb);
-          tma_load_3d(smem_u32(s.Q[st] + KV_SUB * 128), &tQ, 64, r * KV_SUB, bh, fb);
-          tma_load_3d(smem_u32(s.dO[st]), &tdO, 0, r * KV_SUB, bh, fb);
-          tma_load_3d(smem_u32(s.dO[st] + KV_SUB * 128), &tdO, 64, r * KV_SUB, bh, fb);
-          const size_t srow = (size_t)bh * p.Sq_pad + (size_t)r * KV_SUB;
-          bulk_load(smem_u32(s.nlse2[st]), p.nlse2 + srow, KV_SUB * 4, fb);
-          bulk_load(smem_u32(s.delta[st]), p.delta + srow, KV_SUB * 4, fb);
+        }
+        const int cnt = min(32, un.N - n0);
+        for (int k = 0; k < cnt; ++k, ++gn) {
+          const int st = gn % NST;
+          const int rk = __shfl_sync(0xffffffffu, r, k);
+          const int hk = __shfl_sync(0xffffffffu, hh, k);
+          const uint32_t wk = __shfl_sync(0xffffffffu, w, k);
+          if (gn >= NST &&
+              !wait0(smem_u32(&s.bar_q_empty[st]), ((gn / NST) - 1) & 1, TAG_Q_EMPTY)) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            s.step_r[st] = rk;  // published with the loads by the arrive below
+            s.step_hh[st] = hk;
+            s.step_vis[st] = wk;
+            if (!p.test_no_loads) {
+              const int bh = un.b * p.Hq + un.c * p.group + hk;
+              const uint32_t fb = smem_u32(&s.bar_q_full[st]);
+              mbar_arrive_expect_tx(fb, 4 * KV_SUB * 128 + 2 * KV_SUB * 4);
+              tma_load_3d(smem_u32(s.Q[st]), &tQ, 0, rk * KV_SUB, bh, fb);
+              tma_load_3d(smem_u32(s.Q[st] + KV_SUB * 128), &tQ, 64, rk * KV_SUB, bh, fb);
+              tma_load_3d(smem_u32(s.dO[st]), &tdO, 0, rk * KV_SUB, bh, fb);
+              tma_load_3d(smem_u32(s.dO[st] + KV_SUB * 128), &tdO, 64, rk * KV_SUB, bh, fb);
+              const size_t srow = (size_t)bh * p.Sq_pad + (size_t)rk * KV_SUB;
+              bulk_load(smem_u32(s.nlse2[st]), p.nlse2 + srow, KV_SUB * 4, fb);
+              bulk_load(smem_u32(s.delta[st]), p.delta + srow, KV_SUB * 4, fb);
+            }
+          }
+          __syncwarp();
         }
       }
-      if (!ok && !p.test_no_loads) {
-        // the CTA gave up: let the copies still in flight land before it exits
-        if (kv_pending) mbar_drain(kvbar, (up - 1) & 1, wc.timeout_ns);
-        for (int k = gn > NST ? gn - NST : 0; k < gn; ++k)
-          mbar_drain(smem_u32(&s.bar_q_full[k % NST]), (k / NST) & 1, wc.timeout_ns);
-      }
+    }
+    if (!ok && !p.test_no_loads && lane == 0) {
+      // the CTA gave up: let the copies still in flight land before it exits
+      if (kv_pending) mbar_drain(kvbar, (up - 1) & 1, wc.timeout_ns);
+      for (int k = gn > NST ? gn - NST : 0; k < gn; ++k)
+        mbar_drain(smem_u32(&s.bar_q_full[k % NST]), (k / NST) & 1, wc.timeout_ns);
     }
   } else if (warp < SM_WARP0) {
     // ------------------------------------------------------------ MMA issuers (whole warps)
