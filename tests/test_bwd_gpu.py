@@ -49,6 +49,12 @@ CASES = [
     Workload("blocks192x320_bf16", "bf16", B=1, Hq=4, Hkv=2, Sq=1000, Skv=1100,
              mask_kind=MASK_BLOCK, bx=192, by=320, block_pattern="random", density=0.5, sink=True,
              seed=24),
+    # blocks that hold no whole softmax-warp region: the producers publish each
+    # step's mask bits (24 x 40), or the softmax warps read the mask (8 x 8)
+    Workload("blocks24x40_f16", "f16", B=1, Hq=4, Hkv=2, Sq=500, Skv=460, mask_kind=MASK_BLOCK,
+             bx=24, by=40, block_pattern="random", density=0.4, seed=25),
+    Workload("blocks8x8_bf16", "bf16", B=1, Hq=2, Hkv=1, Sq=200, Skv=190, mask_kind=MASK_BLOCK,
+             bx=8, by=8, block_pattern="random", density=0.3, sink=True, seed=26),
 ]
 
 
