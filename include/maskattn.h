@@ -64,7 +64,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* bad shape, null or misaligned pointer, bad mask fields */
-  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement (D != 128) */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request the library does not implement (D != 128) */
   ATTN_ERR_WORKSPACE = 3,   /* ws_bytes smaller than attn_workspace_size() */
   ATTN_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
   ATTN_ERR_TIMEOUT = 5      /* a device-side wait ran out (read back by attn_get_device_status) */
