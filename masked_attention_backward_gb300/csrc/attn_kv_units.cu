@@ -443,10 +443,9 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
       for (int n = 0; n < un.N; ++n, ++gn) {
         const int st = gn % NST, bf = gn & 1;
         const uint32_t colS = COL_BUF + 128 * bf + 16 * g;
-        // s_full implies the stage's loads landed; waiting on q_full as well
-        // makes the bulk-copied rows and the step's coordinates visible
-        // the step's coordinates (and, block masks, the mask bytes its
-        // visibility needs) are read while S^T is still being computed
+        // the stage's loads (and with them the step's coordinates and the
+        // bulk-copied statistics) first: the visibility word is worked out
+        // while S^T is still being computed
         if (!mbar_wait(smem_u32(&s.bar_q_full[st]), (gn / NST) & 1, wc, TAG_Q_FULL)) {
           ok = false;
           break;
