@@ -114,9 +114,33 @@ struct KvUnit {
 
 }  // namespace kvu_side
 
+// The two halves of vis_key_row, for instances that know the mask family
+// (16 queries: the dK/dV softmax warps' share).  Keeping the other family's
+// code out of the softmax loop measured 3 to 4 % faster on short walks.
+__device__ __forceinline__ uint32_t vis_key_row_closed(const AttnParams& p, int j, int i0, int Lq,
+                                                       int Lk) {
+  if (j >= Lk) return 0u;
+  const uint32_t inrange = bit_range(0, Lq - 1 - i0);
+  if (p.mask_kind == MK_NONE) return inrange;
+  if (p.mask_kind == MK_CAUSAL) return inrange & bit_range(j - i0, 31);
+  return inrange & bit_range(j - i0, j + p.window - 1 - i0);
+}
+__device__ __forceinline__ uint32_t vis_key_row_block(const AttnParams& p, int bh, int j, int i0,
+                                                      int Lq, int Lk) {
+  if (j >= Lk) return 0u;
+  const uint8_t* row = p.maskT + ((size_t)bh * p.nkb + j / p.by) * p.nqb;
+  const int iend = min(i0 + 15, Lq - 1);
+  if (iend < i0) return 0u;
+  uint32_t m = 0;
+  for (int qb = i0 / p.bx; qb * p.bx <= iend; ++qb)
+    if (row[qb]) m |= bit_range(qb * p.bx - i0, (qb + 1) * p.bx - 1 - i0);
+  return m & bit_range(0, iend - i0);
+}
+
 // BHSD layout only (the packed layout keeps the per-tile kernel).
 // HILO: P^T and dS^T enter dV and dK as high part + remainder (compensated).
-template <bool BF16, bool HILO>
+// BLOCK: block masks (otherwise the closed-form masks).
+template <bool BF16, bool HILO, bool BLOCK>
 __global__ void __launch_bounds__(kvu_side::NUM_THREADS, 1)
 k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tdO,
              const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
@@ -128,7 +152,7 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
                                      ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int U = p.nKT_k * p.B * p.Hkv;
-  const bool blk_regions = p.mask_kind == MK_BLOCK && (p.by & 31) == 0 && (p.bx & 15) == 0;
+  const bool blk_regions = BLOCK && (p.by & 31) == 0 && (p.bx & 15) == 0;
   WaitCtx wc{p.status, &s.abort_flag, p.timeout_ns};
 
   if (threadIdx.x == 0) {
@@ -459,9 +483,11 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
           vis = ((s.step_vis[st] >> (4 * sp + g)) & 1u) && j < un.Lk
                     ? bit_range(0, un.Lq - 1 - (r * KV_SUB + 16 * g))
                     : 0u;
+        } else if constexpr (BLOCK) {
+          vis = vis_key_row_block(p, un.b * p.Hq + un.c * p.group + s.step_hh[st], j,
+                                  r * KV_SUB + 16 * g, un.Lq, un.Lk);
         } else {
-          vis = vis_key_row(p, un.b * p.Hq + un.c * p.group + s.step_hh[st], j,
-                            r * KV_SUB + 16 * g, un.Lq, un.Lk);
+          vis = vis_key_row_closed(p, j, r * KV_SUB + 16 * g, un.Lq, un.Lk);
         }
         float lv[16];
         load16_shared(&s.nlse2[st][16 * g], lv);
@@ -574,10 +600,13 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
 cudaError_t launch_dkdv_units(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                               const CUtensorMap& tdO, const CUtensorMap& tK,
                               const CUtensorMap& tV, void* dk, void* dv, cudaStream_t st) {
-  using Kern = decltype(&k_dkdv_units<true, false>);
-  static const Kern table[2][2] = {{k_dkdv_units<false, false>, k_dkdv_units<false, true>},
-                                   {k_dkdv_units<true, false>, k_dkdv_units<true, true>}};
-  const Kern kern = table[bf16 ? 1 : 0][p.compensated ? 1 : 0];
+  using Kern = decltype(&k_dkdv_units<true, false, false>);
+  static const Kern table[2][2][2] = {
+      {{k_dkdv_units<false, false, false>, k_dkdv_units<false, false, true>},
+       {k_dkdv_units<false, true, false>, k_dkdv_units<false, true, true>}},
+      {{k_dkdv_units<true, false, false>, k_dkdv_units<true, false, true>},
+       {k_dkdv_units<true, true, false>, k_dkdv_units<true, true, true>}}};
+  const Kern kern = table[bf16 ? 1 : 0][p.compensated ? 1 : 0][p.mask_kind == MK_BLOCK ? 1 : 0];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kvu_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;
