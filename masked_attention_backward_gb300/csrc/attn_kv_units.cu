@@ -114,29 +114,6 @@ struct KvUnit {
 
 }  // namespace kvu_side
 
-// The two halves of vis_key_row, for instances that know the mask family
-// (16 queries: the dK/dV softmax warps' share).  Keeping the other family's
-// code out of the softmax loop measured 3 to 4 % faster on short walks.
-__device__ __forceinline__ uint32_t vis_key_row_closed(const AttnParams& p, int j, int i0, int Lq,
-                                                       int Lk) {
-  if (j >= Lk) return 0u;
-  const uint32_t inrange = bit_range(0, Lq - 1 - i0);
-  if (p.mask_kind == MK_NONE) return inrange;
-  if (p.mask_kind == MK_CAUSAL) return inrange & bit_range(j - i0, 31);
-  return inrange & bit_range(j - i0, j + p.window - 1 - i0);
-}
-__device__ __forceinline__ uint32_t vis_key_row_block(const AttnParams& p, int bh, int j, int i0,
-                                                      int Lq, int Lk) {
-  if (j >= Lk) return 0u;
-  const uint8_t* row = p.maskT + ((size_t)bh * p.nkb + j / p.by) * p.nqb;
-  const int iend = min(i0 + 15, Lq - 1);
-  if (iend < i0) return 0u;
-  uint32_t m = 0;
-  for (int qb = i0 / p.bx; qb * p.bx <= iend; ++qb)
-    if (row[qb]) m |= bit_range(qb * p.bx - i0, (qb + 1) * p.bx - 1 - i0);
-  return m & bit_range(0, iend - i0);
-}
-
 // BHSD layout only (the packed layout keeps the per-tile kernel).
 // HILO: P^T and dS^T enter dV and dK as high part + remainder (compensated).
 // BLOCK: block masks (otherwise the closed-form masks).
