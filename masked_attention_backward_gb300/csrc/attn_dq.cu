@@ -615,7 +615,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         }
         const int t = s.step_t[st];
         // warp-uniform: the whole 128 x 64 sub-tile is visible
-        const bool full = t >= flo && t <= fhi;
+        const bool full = !BLOCK && t >= flo && t <= fhi;  // (block masks: never)
         uint32_t vis;
         if (full) {
           vis = 0xffffffffu;

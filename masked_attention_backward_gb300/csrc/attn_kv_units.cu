@@ -452,7 +452,7 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
           break;
         }
         const int r = s.step_r[st];
-        const bool full = r >= flo && r <= fhi;
+        const bool full = !BLOCK && r >= flo && r <= fhi;  // (block masks: never)
         uint32_t vis;
         if (full) {
           vis = 0xffffu;
