@@ -135,18 +135,19 @@ struct DqUnit {
 
 }  // namespace dq_side
 
-// BLOCK: block masks (otherwise the closed-form masks); each instance keeps
+// MK: the mask kind (MK_NONE, MK_CAUSAL, MK_SLIDING or MK_BLOCK); each instance keeps
 // only its own visibility code in the softmax loop (measured 1.5 to 3.5 %
 // faster on the short-walk and variable-length workloads).
 // HILO: dS enters the dQ contraction as a 16-bit high part (columns
 // 32 g .. 32 g + 15 of group g's slice) plus a 16-bit remainder (columns
 // 32 g + 16 .. 32 g + 31, whose fp32 S values are already in registers).
-template <bool BF16, bool VARLEN, bool HILO, bool BLOCK>
+template <bool BF16, bool VARLEN, bool HILO, int MK>
 __global__ void __launch_bounds__(dq_side::NUM_THREADS, 1)
 k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tdO,
      const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
      uint16_t* __restrict__ dq, const AttnParams p) {
   using namespace dq_side;
+  constexpr bool BLOCK = MK == MK_BLOCK;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -627,7 +628,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
           if constexpr (BLOCK)
             vis = vis_query_row_block(p, un.bh, i, t * Q_SUB + 32 * g, p.Sq, VARLEN ? Lk : p.Skv);
           else
-            vis = vis_query_row_closed(p, i, t * Q_SUB + 32 * g, p.Sq, VARLEN ? Lk : p.Skv);
+            vis = vis_query_row_closed<MK>(p, i, t * Q_SUB + 32 * g, p.Sq, VARLEN ? Lk : p.Skv);
         }
         if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (m >> 1) & 1, wc, TAG_S_FULL)) {
           ok = false;
@@ -696,18 +697,17 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
 cudaError_t launch_dq(bool bf16, const AttnParams& p, const CUtensorMap& tQ, const CUtensorMap& tdO,
                       const CUtensorMap& tK, const CUtensorMap& tV, void* dq, cudaStream_t st) {
   const bool varlen = p.seqlen_q != nullptr || p.seqlen_k != nullptr || p.cu_q != nullptr;
-  using Kern = decltype(&k_dq<true, false, false, false>);
-  static const Kern table[2][2][2][2] = {
-      {{{k_dq<false, false, false, false>, k_dq<false, false, false, true>},
-        {k_dq<false, false, true, false>, k_dq<false, false, true, true>}},
-       {{k_dq<false, true, false, false>, k_dq<false, true, false, true>},
-        {k_dq<false, true, true, false>, k_dq<false, true, true, true>}}},
-      {{{k_dq<true, false, false, false>, k_dq<true, false, false, true>},
-        {k_dq<true, false, true, false>, k_dq<true, false, true, true>}},
-       {{k_dq<true, true, false, false>, k_dq<true, true, false, true>},
-        {k_dq<true, true, true, false>, k_dq<true, true, true, true>}}}};
-  const Kern kern = table[bf16 ? 1 : 0][varlen ? 1 : 0][p.compensated ? 1 : 0]
-                         [p.mask_kind == MK_BLOCK ? 1 : 0];
+  using Kern = decltype(&k_dq<true, false, false, MK_NONE>);
+#define MAB_DQ_ROW(BF, VL, HL)                                                                  \
+  {k_dq<BF, VL, HL, MK_NONE>, k_dq<BF, VL, HL, MK_CAUSAL>, k_dq<BF, VL, HL, MK_SLIDING>,       \
+   k_dq<BF, VL, HL, MK_BLOCK>}
+  static const Kern table[2][2][2][4] = {
+      {{MAB_DQ_ROW(false, false, false), MAB_DQ_ROW(false, false, true)},
+       {MAB_DQ_ROW(false, true, false), MAB_DQ_ROW(false, true, true)}},
+      {{MAB_DQ_ROW(true, false, false), MAB_DQ_ROW(true, false, true)},
+       {MAB_DQ_ROW(true, true, false), MAB_DQ_ROW(true, true, true)}}};
+#undef MAB_DQ_ROW
+  const Kern kern = table[bf16 ? 1 : 0][varlen ? 1 : 0][p.compensated ? 1 : 0][p.mask_kind];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)dq_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;

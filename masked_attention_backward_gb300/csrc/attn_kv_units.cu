@@ -116,14 +116,15 @@ struct KvUnit {
 
 // BHSD layout only (the packed layout keeps the per-tile kernel).
 // HILO: P^T and dS^T enter dV and dK as high part + remainder (compensated).
-// BLOCK: block masks (otherwise the closed-form masks).
-template <bool BF16, bool HILO, bool BLOCK>
+// MK: the mask kind (MK_NONE, MK_CAUSAL, MK_SLIDING or MK_BLOCK).
+template <bool BF16, bool HILO, int MK>
 __global__ void __launch_bounds__(kvu_side::NUM_THREADS, 1)
 k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tdO,
              const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tV,
              uint16_t* __restrict__ dk, uint16_t* __restrict__ dv, const AttnParams p) {
   using namespace kvu_side;
   constexpr int NST = STAGES;
+  constexpr bool BLOCK = MK == MK_BLOCK;
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -464,7 +465,7 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
           vis = vis_key_row_block(p, un.b * p.Hq + un.c * p.group + s.step_hh[st], j,
                                   r * KV_SUB + 16 * g, un.Lq, un.Lk);
         } else {
-          vis = vis_key_row_closed(p, j, r * KV_SUB + 16 * g, un.Lq, un.Lk);
+          vis = vis_key_row_closed<MK>(p, j, r * KV_SUB + 16 * g, un.Lq, un.Lk);
         }
         float lv[16];
         load16_shared(&s.nlse2[st][16 * g], lv);
@@ -577,13 +578,14 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
 cudaError_t launch_dkdv_units(bool bf16, const AttnParams& p, const CUtensorMap& tQ,
                               const CUtensorMap& tdO, const CUtensorMap& tK,
                               const CUtensorMap& tV, void* dk, void* dv, cudaStream_t st) {
-  using Kern = decltype(&k_dkdv_units<true, false, false>);
-  static const Kern table[2][2][2] = {
-      {{k_dkdv_units<false, false, false>, k_dkdv_units<false, false, true>},
-       {k_dkdv_units<false, true, false>, k_dkdv_units<false, true, true>}},
-      {{k_dkdv_units<true, false, false>, k_dkdv_units<true, false, true>},
-       {k_dkdv_units<true, true, false>, k_dkdv_units<true, true, true>}}};
-  const Kern kern = table[bf16 ? 1 : 0][p.compensated ? 1 : 0][p.mask_kind == MK_BLOCK ? 1 : 0];
+  using Kern = decltype(&k_dkdv_units<true, false, MK_NONE>);
+#define MAB_KVU_ROW(BF, HL)                                                                     \
+  {k_dkdv_units<BF, HL, MK_NONE>, k_dkdv_units<BF, HL, MK_CAUSAL>,                              \
+   k_dkdv_units<BF, HL, MK_SLIDING>, k_dkdv_units<BF, HL, MK_BLOCK>}
+  static const Kern table[2][2][4] = {{MAB_KVU_ROW(false, false), MAB_KVU_ROW(false, true)},
+                                      {MAB_KVU_ROW(true, false), MAB_KVU_ROW(true, true)}};
+#undef MAB_KVU_ROW
+  const Kern kern = table[bf16 ? 1 : 0][p.compensated ? 1 : 0][p.mask_kind];
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kvu_side::SMEM_BYTES);
   if (e != cudaSuccess) return e;

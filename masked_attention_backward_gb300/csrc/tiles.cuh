@@ -70,13 +70,14 @@ __device__ __forceinline__ uint32_t vis_key_row(const AttnParams& p, int bh, int
 // (16 queries: the dK/dV softmax warps' share).  Keeping the other family's
 // code out of the softmax loop measured 3 to 4 % faster on short walks in the
 // persistent dK/dV kernel.
+template <int MK>
 __device__ __forceinline__ uint32_t vis_key_row_closed(const AttnParams& p, int j, int i0, int Lq,
                                                        int Lk) {
   if (j >= Lk) return 0u;
   const uint32_t inrange = bit_range(0, Lq - 1 - i0);
-  if (p.mask_kind == MK_NONE) return inrange;
-  if (p.mask_kind == MK_CAUSAL) return inrange & bit_range(j - i0, 31);
-  return inrange & bit_range(j - i0, j + p.window - 1 - i0);
+  if constexpr (MK == MK_NONE) return inrange;
+  else if constexpr (MK == MK_CAUSAL) return inrange & bit_range(j - i0, 31);
+  else return inrange & bit_range(j - i0, j + p.window - 1 - i0);
 }
 __device__ __forceinline__ uint32_t vis_key_row_block(const AttnParams& p, int bh, int j, int i0,
                                                       int Lq, int Lk) {
@@ -92,13 +93,14 @@ __device__ __forceinline__ uint32_t vis_key_row_block(const AttnParams& p, int b
 
 // The two halves of vis_query_row, for instances that know the mask family
 // (32 keys: a dQ softmax warp's share).
+template <int MK>
 __device__ __forceinline__ uint32_t vis_query_row_closed(const AttnParams& p, int i, int j0,
                                                          int Lq, int Lk) {
   if (i >= Lq) return 0u;
   const uint32_t inrange = bit_range(0, Lk - 1 - j0);
-  if (p.mask_kind == MK_NONE) return inrange;
-  if (p.mask_kind == MK_CAUSAL) return inrange & bit_range(0, i - j0);
-  return inrange & bit_range(i - p.window + 1 - j0, i - j0);
+  if constexpr (MK == MK_NONE) return inrange;
+  else if constexpr (MK == MK_CAUSAL) return inrange & bit_range(0, i - j0);
+  else return inrange & bit_range(i - p.window + 1 - j0, i - j0);
 }
 __device__ __forceinline__ uint32_t vis_query_row_block(const AttnParams& p, int bh, int i, int j0,
                                                         int Lq, int Lk) {
