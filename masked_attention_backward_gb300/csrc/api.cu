@@ -193,6 +193,8 @@ AttnParams params_of(const attn_shape_t* sh, const attn_mask_desc_t* mk, const W
   p.window = mk->kind == ATTN_MASK_SLIDING ? mk->window : 0;
   p.bx = mk->kind == ATTN_MASK_BLOCK ? mk->bx : 1;
   p.by = mk->kind == ATTN_MASK_BLOCK ? mk->by : 1;
+  p.inv_bx = 1.0f / (float)p.bx;
+  p.inv_by = 1.0f / (float)p.by;
   p.nqb = d.nqb;
   p.nkb = d.nkb;
   if (mk->kind == ATTN_MASK_BLOCK) {

@@ -440,6 +440,12 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
       un.init(p, u);
       if (un.N == 0) continue;
       const int j = un.k0 + rloc;
+      // block masks: this lane's row of the transposed mask for the unit's
+      // first query head (the step's head adds whole heads)
+      const uint8_t* rowT =
+          BLOCK ? p.maskT + ((size_t)(un.b * p.Hq + un.c * p.group) * p.nkb + min(j, p.Skv - 1) / p.by) *
+                                p.nqb
+                : nullptr;
       int flo, fhi;  // query sub-tiles that are entirely visible
       full_range_kv(p.mask_kind, p.window, un.Lq, un.Lk, un.k0, &flo, &fhi);
       for (int n = 0; n < un.N; ++n, ++gn) {
@@ -462,8 +468,21 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
                     ? bit_range(0, un.Lq - 1 - (r * KV_SUB + 16 * g))
                     : 0u;
         } else if constexpr (BLOCK) {
-          vis = vis_key_row_block(p, un.b * p.Hq + un.c * p.group + s.step_hh[st], j,
-                                  r * KV_SUB + 16 * g, un.Lq, un.Lk);
+          {
+            // key j against queries i0 .. i0 + 15 (the lane's mask row is
+            // found once per unit; the query-block quotient by a reciprocal,
+            // measured 10 % faster on bigbird than the division per step)
+            const uint8_t* row = rowT + (size_t)s.step_hh[st] * p.nkb * p.nqb;
+            const int i0 = r * KV_SUB + 16 * g;
+            const int iend = min(i0 + 15, un.Lq - 1);
+            uint32_t m = 0;
+            if (j < un.Lk && iend >= i0) {
+              for (int qb = div_by(i0, p.bx, p.inv_bx); qb * p.bx <= iend; ++qb)
+                if (row[qb]) m |= bit_range(qb * p.bx - i0, (qb + 1) * p.bx - 1 - i0);
+              m &= bit_range(0, iend - i0);
+            }
+            vis = m;
+          }
         } else {
           vis = vis_key_row_closed<MK>(p, j, r * KV_SUB + 16 * g, un.Lq, un.Lk);
         }

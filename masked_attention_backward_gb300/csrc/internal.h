@@ -43,6 +43,7 @@ struct WsLayout {
 struct AttnParams {
   int B, Hq, Hkv, Sq, Skv, group, Sq_pad;
   int mask_kind, window, bx, by, nqb, nkb;
+  float inv_bx, inv_by;  // 1 / bx, 1 / by (block masks; quotients corrected to exact)
   const uint8_t* mask;   // [B*Hq, nqb, nkb]
   const uint8_t* maskT;  // [B*Hq, nkb, nqb]
   const int* sel_k;

@@ -7,6 +7,16 @@
 
 namespace mab {
 
+// a / b for 0 <= a < 2^24 and b >= 1, given inv_b = 1 / b rounded to float:
+// the float quotient is within 2 / b of a / b (exact for b = 1, 2), so one
+// correction each way gives the exact floor.
+__device__ __forceinline__ int div_by(int a, int b, float inv_b) {
+  int q = __float2int_rz((float)a * inv_b);
+  q += (q + 1) * b <= a ? 1 : 0;
+  q -= q * b > a ? 1 : 0;
+  return q;
+}
+
 // Bits [lo, hi] (inclusive, clipped to [0, 31]) set.
 __device__ __forceinline__ uint32_t bit_range(int lo, int hi) {
   if (lo < 0) lo = 0;
@@ -66,8 +76,8 @@ __device__ __forceinline__ uint32_t vis_key_row(const AttnParams& p, int bh, int
   }
 }
 
-// The two halves of vis_key_row, for instances that know the mask family
-// (16 queries: the dK/dV softmax warps' share).  Keeping the other family's
+// The closed-form half of vis_key_row, for instances that know the mask kind
+// (16 queries: the dK/dV softmax warps' share).  Keeping the other kinds'
 // code out of the softmax loop measured 3 to 4 % faster on short walks in the
 // persistent dK/dV kernel.
 template <int MK>
@@ -79,18 +89,6 @@ __device__ __forceinline__ uint32_t vis_key_row_closed(const AttnParams& p, int 
   else if constexpr (MK == MK_CAUSAL) return inrange & bit_range(j - i0, 31);
   else return inrange & bit_range(j - i0, j + p.window - 1 - i0);
 }
-__device__ __forceinline__ uint32_t vis_key_row_block(const AttnParams& p, int bh, int j, int i0,
-                                                      int Lq, int Lk) {
-  if (j >= Lk) return 0u;
-  const uint8_t* row = p.maskT + ((size_t)bh * p.nkb + j / p.by) * p.nqb;
-  const int iend = min(i0 + 15, Lq - 1);
-  if (iend < i0) return 0u;
-  uint32_t m = 0;
-  for (int qb = i0 / p.bx; qb * p.bx <= iend; ++qb)
-    if (row[qb]) m |= bit_range(qb * p.bx - i0, (qb + 1) * p.bx - 1 - i0);
-  return m & bit_range(0, iend - i0);
-}
-
 // The two halves of vis_query_row, for instances that know the mask family
 // (32 keys: a dQ softmax warp's share).
 template <int MK>
