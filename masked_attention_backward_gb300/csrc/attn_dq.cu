@@ -568,6 +568,9 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
       const size_t srow = (size_t)un.bh * p.Sq_pad + i;
       const float nlse2_i = p.nlse2[srow];  // -lse log2(e)
       const float delta_i = p.delta[srow];
+      // block masks: this row's mask row, found once per unit
+      const uint8_t* rowM =
+          BLOCK ? p.mask + ((size_t)un.bh * p.nqb + min(i, p.Sq - 1) / p.bx) * p.nkb : nullptr;
       // Q and dO rows of the unit into TMEM as 16-bit pairs (element 2c in
       // the low half of column c): this warp copies d columns
       // 64 g .. 64 g + 63 of its rows.  Every S / dP MMA of the previous unit
@@ -625,10 +628,21 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
                     ? bit_range(0, (VARLEN ? Lk : p.Skv) - 1 - (t * Q_SUB + 32 * g))
                     : 0u;
         } else {
-          if constexpr (BLOCK)
-            vis = vis_query_row_block(p, un.bh, i, t * Q_SUB + 32 * g, p.Sq, VARLEN ? Lk : p.Skv);
-          else
+          if constexpr (BLOCK) {
+            // row i against keys j0 .. j0 + 31; the key-block quotient by a
+            // reciprocal
+            const int j0 = t * Q_SUB + 32 * g;
+            const int jend = min(j0 + 31, (VARLEN ? Lk : p.Skv) - 1);
+            uint32_t bits = 0;
+            if (i < p.Sq && jend >= j0) {
+              for (int kb = div_by(j0, p.by, p.inv_by); kb * p.by <= jend; ++kb)
+                if (rowM[kb]) bits |= bit_range(kb * p.by - j0, (kb + 1) * p.by - 1 - j0);
+              bits &= bit_range(0, jend - j0);
+            }
+            vis = bits;
+          } else {
             vis = vis_query_row_closed<MK>(p, i, t * Q_SUB + 32 * g, p.Sq, VARLEN ? Lk : p.Skv);
+          }
         }
         if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (m >> 1) & 1, wc, TAG_S_FULL)) {
           ok = false;

@@ -89,8 +89,8 @@ __device__ __forceinline__ uint32_t vis_key_row_closed(const AttnParams& p, int 
   else if constexpr (MK == MK_CAUSAL) return inrange & bit_range(j - i0, 31);
   else return inrange & bit_range(j - i0, j + p.window - 1 - i0);
 }
-// The two halves of vis_query_row, for instances that know the mask family
-// (32 keys: a dQ softmax warp's share).
+// The closed-form half of vis_query_row, for instances that know the mask
+// kind (32 keys: a dQ softmax warp's share).
 template <int MK>
 __device__ __forceinline__ uint32_t vis_query_row_closed(const AttnParams& p, int i, int j0,
                                                          int Lq, int Lk) {
@@ -99,17 +99,6 @@ __device__ __forceinline__ uint32_t vis_query_row_closed(const AttnParams& p, in
   if constexpr (MK == MK_NONE) return inrange;
   else if constexpr (MK == MK_CAUSAL) return inrange & bit_range(0, i - j0);
   else return inrange & bit_range(i - p.window + 1 - j0, i - j0);
-}
-__device__ __forceinline__ uint32_t vis_query_row_block(const AttnParams& p, int bh, int i, int j0,
-                                                        int Lq, int Lk) {
-  if (i >= Lq) return 0u;
-  const uint8_t* row = p.mask + ((size_t)bh * p.nqb + i / p.bx) * p.nkb;
-  const int jend = min(j0 + 31, Lk - 1);
-  if (jend < j0) return 0u;
-  uint32_t m = 0;
-  for (int kb = j0 / p.by; kb * p.by <= jend; ++kb)
-    if (row[kb]) m |= bit_range(kb * p.by - j0, (kb + 1) * p.by - 1 - j0);
-  return m & bit_range(0, jend - j0);
 }
 
 // The sub-tiles of a walk that are entirely visible form one contiguous
