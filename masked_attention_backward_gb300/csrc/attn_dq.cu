@@ -251,10 +251,10 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
             uint32_t mv[8];
             if (blk_regions) {
               const uint8_t* mb = p.mask + (size_t)un.bh * p.nqb * p.nkb;
-  #pragma unroll
+#pragma unroll
               for (int sp2 = 0; sp2 < 4; ++sp2) {
                 const int qb = min((un.q0 + 32 * sp2) / p.bx, p.nqb - 1);
-  #pragma unroll
+#pragma unroll
                 for (int g2 = 0; g2 < 2; ++g2) {
                   const int kb = min((t * Q_SUB + 32 * g2) / p.by, p.nkb - 1);
                   mv[2 * sp2 + g2] = mb[(size_t)qb * p.nkb + kb];
@@ -270,7 +270,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
             s.step_t[st] = t;  // published by the arrive below together with the loads
             if (blk_regions) {
               uint32_t w = 0;
-  #pragma unroll
+#pragma unroll
               for (int e = 0; e < 8; ++e)
                 if (mv[e] && un.q0 + 32 * (e >> 1) < p.Sq && t * Q_SUB + 32 * (e & 1) < p.Skv)
                   w |= 1u << e;
@@ -359,16 +359,16 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
                 // (indices clamped into the mask, ranges applied after)
                 const uint8_t* mb = p.mask + (size_t)un.bh * p.nqb * p.nkb;
                 uint32_t mv[8];
-    #pragma unroll
+#pragma unroll
                 for (int sp2 = 0; sp2 < 4; ++sp2) {
                   const int qb = min((un.q0 + 32 * sp2) / p.bx, p.nqb - 1);
-    #pragma unroll
+#pragma unroll
                   for (int g2 = 0; g2 < 2; ++g2) {
                     const int kb = min((t * Q_SUB + 32 * g2) / p.by, p.nkb - 1);
                     mv[2 * sp2 + g2] = mb[(size_t)qb * p.nkb + kb];
                   }
                 }
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < 8; ++e)
                   if (mv[e] && un.q0 + 32 * (e >> 1) < p.Sq && t * Q_SUB + 32 * (e & 1) < p.Skv)
                     w |= 1u << e;
@@ -642,6 +642,31 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
             vis = bits;
           } else {
             vis = vis_query_row_closed<MK>(p, i, t * Q_SUB + 32 * g, p.Sq, VARLEN ? Lk : p.Skv);
+          }
+        }
+        if constexpr (!VARLEN) {
+          // no key of the warp's region is visible for any of its rows: dS is
+          // zero, written without loading S or dP once both MMAs completed
+          // (not in the per-batch-length instances, whose registers are at
+          // their limit)
+          if (!full && __all_sync(0xffffffffu, vis == 0u)) {
+            if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (m >> 1) & 1, wc, TAG_S_FULL)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            uint32_t z[HILO ? 32 : 16];
+#pragma unroll
+            for (int c = 0; c < (HILO ? 32 : 16); ++c) z[c] = 0u;
+            if constexpr (HILO)
+              tmem_st32(lane_base + COL_BUF + bf * 128 + 32 * g, z);
+            else
+              tmem_st16(lane_base + COL_BUF + bf * 128 + 32 * g, z);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&s.bar_p_full[bf]));
+            continue;
           }
         }
         if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (m >> 1) & 1, wc, TAG_S_FULL)) {

@@ -112,6 +112,17 @@ struct KvUnit {
   }
 };
 
+// Zero P^T (or dS^T) of a softmax warp's 16 columns at TMEM address `taddr`
+// (and, compensated, a zero remainder over the next 8), then waits for the
+// store: the packed values of a region none of whose logits is visible.
+template <bool HILO>
+__device__ __forceinline__ void kv_write_zero(uint32_t taddr) {
+  const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+  tmem_st8(taddr, z);
+  if constexpr (HILO) tmem_st8(taddr + 8, z);
+  tmem_wait_st();
+}
+
 }  // namespace kvu_side
 
 // BHSD layout only (the packed layout keeps the per-tile kernel).
@@ -486,6 +497,10 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
         } else {
           vis = vis_key_row_closed<MK>(p, j, r * KV_SUB + 16 * g, un.Lq, un.Lk);
         }
+        // no logit of the warp's region is visible: P^T and dS^T are zero
+        // (written without loading S^T or dP^T, once the MMA that writes
+        // those columns has completed)
+        const bool none = !full && __all_sync(0xffffffffu, vis == 0u);
         float lv[16];
         load16_shared(&s.nlse2[st][16 * g], lv);
         if (!mbar_wait(smem_u32(&s.bar_s_full[bf]), (gn >> 1) & 1, wc, TAG_S_FULL)) {
@@ -493,11 +508,15 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
           break;
         }
         tc_fence_after();
-        float sv[16];
-        tmem_ld16(lane_base + colS, sv);
-        tmem_wait_ld_regs(sv);
         float pv[16];
-        kv_write_p<BF16, HILO>(lane_base + colS, sv, lv, full, vis, p.scale_log2, pv);
+        if (none) {
+          kv_write_zero<HILO>(lane_base + colS);
+        } else {
+          float sv[16];
+          tmem_ld16(lane_base + colS, sv);
+          tmem_wait_ld_regs(sv);
+          kv_write_p<BF16, HILO>(lane_base + colS, sv, lv, full, vis, p.scale_log2, pv);
+        }
         warp_arrive(&s.bar_p_full[bf]);
 
         float dl[16];
@@ -507,11 +526,15 @@ k_dkdv_units(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUt
           break;
         }
         tc_fence_after();
-        float dp[16];
-        tmem_ld16(lane_base + colS + 64, dp);
-        tmem_wait_ld_regs(dp);
-        uint32_t pk[8];
-        kv_write_ds<BF16, HILO>(lane_base + colS + 64, pv, dp, dl, pk);
+        if (none) {
+          kv_write_zero<HILO>(lane_base + colS + 64);
+        } else {
+          float dp[16];
+          tmem_ld16(lane_base + colS + 64, dp);
+          tmem_wait_ld_regs(dp);
+          uint32_t pk[8];
+          kv_write_ds<BF16, HILO>(lane_base + colS + 64, pv, dp, dl, pk);
+        }
         warp_arrive(&s.bar_ds_full[bf]);
       }
     }
