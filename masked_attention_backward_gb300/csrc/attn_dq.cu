@@ -675,6 +675,8 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
         }
         tc_fence_after();
         const uint32_t col = COL_BUF + bf * 128 + 32 * g;
+        // every key of the region visible for every row: no masking
+        const bool fullw = full || (!VARLEN && __all_sync(0xffffffffu, vis == 0xffffffffu));
         float sv[32], dp[32];
         tmem_ld32(lane_base + col, sv);
         tmem_ld32(lane_base + col + 64, dp);
@@ -690,7 +692,7 @@ k_dq(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap
             pk[(HILO ? 16 : 0) + c] = pack2<BF16>(d0 - h.x, d1 - h.y);
           }
         };
-        if (full) {
+        if (fullw) {
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const float p0 = fast_exp2(fmaf(sv[2 * c], p.scale_log2, nlse2_i));
