@@ -48,6 +48,12 @@ KERNEL_SOURCES = {
 }
 
 
+def parse_runs(text: str):
+    """--e2e-chunks: "8" (equal runs) or "1,3,3,1" (key/value heads per run)."""
+    parts = [int(x) for x in text.split(",")]
+    return parts[0] if len(parts) == 1 else parts
+
+
 def kernel_hash(name: str) -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES.get(name, []):
@@ -294,7 +300,7 @@ def run_ours(args, rank, world, local):
         e2e = {"value": round(world * fl["total"] * args.steps / (te * 1e-3) / 1e12, 2),
                "unit": "TFLOP/s", "ms_per_step": round(te / args.steps, 3),
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "pipeline_chunks": hb.chunks}
+               "pipeline_chunks": hb.chunks, "pipeline_runs": hb.sizes}
         # the same gradients as the device-resident calls timed above
         for a, b_ in zip(host_out, out):
             if a is not None and not torch.equal(a, b_.cpu()):
@@ -630,8 +636,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--compensated", action="store_true",
                     help="time the compensated backward (P and dS as high part + remainder)")
-    ap.add_argument("--e2e-chunks", type=int, default=8,
-                    help="runs of GQA groups the host-buffer pipeline overlaps")
+    ap.add_argument("--e2e-chunks", type=parse_runs, default=8,
+                    help="runs of GQA groups the host-buffer pipeline overlaps: a count of "
+                         "equal runs, or the key/value heads of each run (e.g. 1,3,3,1)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -290,7 +290,10 @@ class HostBackward:
     host<->device copies overlapped with the kernels.
 
     The heads of a GQA group are independent of every other group, so the
-    call is split into `chunks` runs of whole key/value heads.  Chunk c's
+    call is split into runs of whole key/value heads: `chunks` equal runs, or
+    a list of the key/value heads in each run (a short first run shortens the
+    copy nothing hides, a short last run the copy out that follows the last
+    kernel, and longer runs in between leave fewer grid tails).  Chunk c's
     inputs are copied in on one stream while earlier chunks run attn_bwd and
     their gradients are copied out on another; every chunk is one attn_bwd
     call on pointer offsets into device buffers that are allocated once here
@@ -307,15 +310,21 @@ class HostBackward:
     whole call."""
 
     def __init__(self, B, Hq, Hkv, Sq, Skv, dtype, mask: Mask, scale: float, has_sink: bool,
-                 device, chunks: int = 8, compensated: bool = False):
+                 device, chunks=8, compensated: bool = False):
         self.B, self.Hq, self.Hkv, self.Sq, self.Skv = B, Hq, Hkv, Sq, Skv
         self.dtype, self.mask, self.scale, self.has_sink = dtype, mask, scale, has_sink
         self.device = torch.device(device)
-        if B != 1 or Hkv % chunks != 0:
-            chunks = 1
-        self.chunks = chunks
+        if isinstance(chunks, int):
+            sizes = [Hkv // chunks] * chunks if chunks > 0 and Hkv % chunks == 0 else [Hkv]
+        else:
+            sizes = [int(x) for x in chunks]
+            if any(x <= 0 for x in sizes) or sum(sizes) != Hkv:
+                raise ValueError(f"runs of key/value heads {sizes} do not cover the {Hkv} heads")
+        if B != 1:
+            sizes = [Hkv]
+        self.sizes = sizes
+        self.chunks = len(sizes)
         self.g = Hq // Hkv
-        kvc = Hkv // chunks
         D = 128
         e = dict(dtype=dtype, device=self.device)
         self.dev = {
@@ -330,14 +339,17 @@ class HostBackward:
             self.dev["sink"] = torch.empty(Hq, dtype=torch.float32, device=self.device)
             self.dev["dsink"] = torch.empty(Hq, dtype=torch.float32, device=self.device)
         code = ATTN_BF16 if dtype == torch.bfloat16 else ATTN_F16
-        self.cshape = attn_shape_t(B, Hq // chunks, kvc, Sq, Skv, D, code,
-                                   ATTN_FLAG_COMPENSATED if compensated else 0)
-        self.ws = [workspace(self.cshape, mask, self.device) for _ in range(min(3, chunks))]
-        self.s_comp = [torch.cuda.Stream(self.device) for _ in range(min(3, chunks))]
+        flags = ATTN_FLAG_COMPENSATED if compensated else 0
+        self.cshapes = [attn_shape_t(B, self.g * kv, kv, Sq, Skv, D, code, flags) for kv in sizes]
+        nws = min(3, self.chunks)
+        # each workspace is sized for the largest run, so any run may use it
+        big = attn_shape_t(B, self.g * max(sizes), max(sizes), Sq, Skv, D, code, flags)
+        self.ws = [workspace(big, mask, self.device) for _ in range(nws)]
+        self.s_comp = [torch.cuda.Stream(self.device) for _ in range(nws)]
         self.s_in = torch.cuda.Stream(self.device)
         self.s_out = torch.cuda.Stream(self.device)
-        self.ev_in = [torch.cuda.Event() for _ in range(chunks)]
-        self.ev_done = [torch.cuda.Event() for _ in range(chunks)]
+        self.ev_in = [torch.cuda.Event() for _ in range(self.chunks)]
+        self.ev_done = [torch.cuda.Event() for _ in range(self.chunks)]
         self.ev_start = torch.cuda.Event()
         self.ev_out = torch.cuda.Event()
         self.ev_comp = [torch.cuda.Event() for _ in range(len(self.s_comp))]
@@ -355,11 +367,13 @@ class HostBackward:
         self.s_in.wait_event(self.ev_start)
         for sc in self.s_comp:
             sc.wait_event(self.ev_start)
-        C, g = self.chunks, self.g
-        hq, hk = self.Hq // C, self.Hkv // C
+        g = self.g
         d = self.dev
-        for c in range(C):
-            qs, ks = slice(c * hq, (c + 1) * hq), slice(c * hk, (c + 1) * hk)
+        k_lo = 0
+        for c, kv in enumerate(self.sizes):
+            ks = slice(k_lo, k_lo + kv)
+            qs = slice(k_lo * g, (k_lo + kv) * g)
+            k_lo += kv
             with torch.cuda.stream(self.s_in):
                 for n in ("q", "o", "dO", "lse"):
                     d[n][:, qs].copy_(host_in[n][:, qs], non_blocking=True)
@@ -377,7 +391,7 @@ class HostBackward:
                             mask.seqlen_q, mask.seqlen_k)
             sink = d["sink"][qs] if self.has_sink else None
             dsink = d["dsink"][qs] if self.has_sink else None
-            r = attn_bwd(self.cshape, _ptr(d["q"][:, qs]), _ptr(d["k"][:, ks]),
+            r = attn_bwd(self.cshapes[c], _ptr(d["q"][:, qs]), _ptr(d["k"][:, ks]),
                          _ptr(d["v"][:, ks]), _ptr(d["o"][:, qs]), _ptr(d["dO"][:, qs]),
                          _ptr(d["lse"][:, qs]), _ptr(sink), mask.desc(), self.scale,
                          _ptr(d["dq"][:, qs]), _ptr(d["dk"][:, ks]), _ptr(d["dv"][:, ks]),

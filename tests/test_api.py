@@ -183,3 +183,11 @@ def test_visible_pair_count_matches_oracle():
                             seqlen_k=None if inp.seqlen_k is None else inp.seqlen_k.numpy())
         assert (measure.visible_pairs(wl, inp.block_mask, inp.seqlen_q, inp.seqlen_k)
                 == oracle.count_visible(pb)), wl.name
+
+
+def test_host_pipeline_runs_validation():
+    # uneven runs must cover the key/value heads exactly (checked before any allocation)
+    for runs in ([1, 2], [2, 2, 1], [0, 4], [-1, 5]):
+        with pytest.raises(ValueError):
+            mab.HostBackward(1, 8, 4, 64, 64, None, mab.Mask(), 0.088, False, "cpu",
+                             chunks=runs)

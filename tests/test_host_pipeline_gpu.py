@@ -3,7 +3,7 @@ groups overlap the kernels of the previous run, each run being one attn_bwd
 call on pointer offsets.  Its gradients must be bitwise those of a single
 attn_bwd on device-resident inputs (heads are independent and every kernel
 reduces in a fixed order), for several chunk counts and for a block mask
-sliced per run; with B > 1 the call is not split."""
+sliced per run, with equal and with uneven runs; with B > 1 the call is not split."""
 import pytest
 import torch
 
@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     (Workload("pipe_causal_sink_bf16", "bf16", B=1, Hq=8, Hkv=4, Sq=384, Skv=384,
-              mask_kind=MASK_CAUSAL, sink=True, seed=81), [1, 2, 4]),
+              mask_kind=MASK_CAUSAL, sink=True, seed=81), [1, 2, 4, [1, 2, 1], [3, 1]]),
     (Workload("pipe_blocks_f16", "f16", B=1, Hq=4, Hkv=2, Sq=333, Skv=290, mask_kind=MASK_BLOCK,
               bx=48, by=80, block_pattern="random", density=0.4, sink=True, seed=82), [2]),
     (Workload("pipe_swa_b2_bf16", "bf16", B=2, Hq=4, Hkv=2, Sq=300, Skv=300,
@@ -42,7 +42,8 @@ def test_host_pipeline_matches_device_call(cuda_lib, wl, chunk_list):
                     for t in ref]
         hb = mab.HostBackward(wl.B, wl.Hq, wl.Hkv, wl.Sq, wl.Skv, d["q"].dtype, mask, wl.scale,
                               sink is not None, dev, chunks=chunks)
-        assert hb.chunks == (1 if wl.B > 1 else chunks)
+        runs = chunks if isinstance(chunks, list) else [wl.Hkv // chunks] * chunks
+        assert hb.sizes == ([wl.Hkv] if wl.B > 1 else runs)
         for _ in range(2):  # twice: nothing may depend on what the previous call left
             hb(host_in, host_out)
             torch.cuda.synchronize()
