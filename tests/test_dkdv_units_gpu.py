@@ -86,9 +86,18 @@ def test_units_varlen_and_empty_key_tiles(cuda_lib, monkeypatch):
     assert torch.all(units.dk[1, :, 300:].cpu() == 0) and torch.all(units.dv[2].cpu() == 0)
 
 
-def test_units_compensated_equal_to_tile(cuda_lib, monkeypatch):
-    wl = Workload("swa_comp_units", "f16", B=1, Hq=4, Hkv=2, Sq=600, Skv=600,
-                  mask_kind=MASK_SLIDING, window=128, sink=True, seed=74)
+COMPENSATED = [
+    Workload("swa_comp_units", "f16", B=1, Hq=4, Hkv=2, Sq=600, Skv=600,
+             mask_kind=MASK_SLIDING, window=128, sink=True, seed=74),
+    # 64 x 64 blocks: whole softmax-warp regions masked (zero high and low parts)
+    Workload("blocks_comp_units", "f16", B=1, Hq=4, Hkv=4, Sq=700, Skv=650,
+             mask_kind=MASK_BLOCK, bx=64, by=64, block_pattern="random", density=0.35,
+             sink=True, seed=75),
+]
+
+
+@pytest.mark.parametrize("wl", COMPENSATED, ids=[w.name for w in COMPENSATED])
+def test_units_compensated_equal_to_tile(cuda_lib, monkeypatch, wl):
     inp = make_inputs(wl)
     pb = oracle_problem(wl, inp)
     O, lse = forward_stats(wl, inp, pb)
