@@ -409,9 +409,10 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
 
   std::unique_lock<std::mutex> lock(g_prof.mu, std::defer_lock);
   const bool prof = prof_lock(lock);
-  cudaError_t e = cudaMemsetAsync(w + L.status, 0, sizeof(DevStatus), st);
-  if (e == cudaSuccess && single)
-    e = cudaMemsetAsync(w + L.dq_flag, 0, L.dq_part - L.dq_flag, st);
+  // the status word is zeroed by the preprocess kernel, which every call runs
+  // before any kernel that reads or writes it
+  cudaError_t e = cudaSuccess;
+  if (single) e = cudaMemsetAsync(w + L.dq_flag, 0, L.dq_part - L.dq_flag, st);
   // block masks: the tables first, and the preprocess grid beside them (it
   // reads nothing of theirs; its completion implies theirs)
   const bool blk = mask->kind == ATTN_MASK_BLOCK;
@@ -425,7 +426,8 @@ attn_status_t attn_bwd(const attn_shape_t* shape, const void* q, const void* k, 
                           reinterpret_cast<float*>(w + L.delta),
                           reinterpret_cast<float*>(w + L.dsink_part), shape->B, shape->Hq,
                           shape->Sq, d.Sq_pad, mask->seqlen_q, mask->cu_seqlens_q,
-                          mask->total_q, blk && !prof, st);
+                          mask->total_q, reinterpret_cast<DevStatus*>(w + L.status),
+                          blk && !prof, st);
   }
   if (e == cudaSuccess && single) {
     {

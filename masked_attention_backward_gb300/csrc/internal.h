@@ -160,7 +160,7 @@ __device__ __forceinline__ int rows_to_store_k(const AttnParams& p, int b, int r
 cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const float* lse,
                               const float* sink, float* nlse2, float* delta, float* part, int B,
                               int Hq, int Sq, int Sq_pad, const int* seqlen_q, const int* cu_q,
-                              int total_q, bool overlap_prev, cudaStream_t st);
+                              int total_q, DevStatus* status, bool overlap_prev, cudaStream_t st);
 cudaError_t launch_dsink_finalize(const float* part, int Hq, int nparts, float* dsink,
                                   cudaStream_t st);
 cudaError_t launch_mask_tables(const AttnParams& p, uint8_t* maskT, int* sel_k, int* cnt_k,

@@ -30,7 +30,7 @@ k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
              const float* __restrict__ lse, const float* __restrict__ sink,
              float* __restrict__ nlse2, float* __restrict__ delta, float* __restrict__ part, int Hq,
              int Sq, int Sq_pad, int nparts, const int* __restrict__ seqlen_q,
-             const int* __restrict__ cu_q, int total_q) {
+             const int* __restrict__ cu_q, int total_q, DevStatus* __restrict__ status) {
   constexpr int ROWS_PER_WARP = PREP_BLOCK_ROWS / 8;  // 8
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = lane >> 4, l16 = lane & 15;
@@ -42,6 +42,11 @@ k_preprocess(const uint4* __restrict__ O, const uint4* __restrict__ dO,
   // serialization) may be scheduled once every block of this grid has
   // started; it waits for this grid's completion before it reads any result
   grid_launch_dependents();
+  // the call's status word starts at zero: every kernel that reads or writes
+  // it runs after this grid has completed (in stream order, or behind a wait
+  // for this grid), and the table kernel beside it does not touch it
+  if (blk == 0 && bh == 0 && threadIdx.x < sizeof(DevStatus) / sizeof(unsigned int))
+    reinterpret_cast<unsigned int*>(status)[threadIdx.x] = 0u;
   // rows past the batch's length are outside the problem: treated like the
   // padding (Delta 0, -lse log2 e = -inf, no dSink term)
   const int Lq = cu_q ? packed_len(cu_q, b, total_q, Sq)
@@ -215,7 +220,7 @@ k_mask_tables(const AttnParams p, uint8_t* __restrict__ maskT, int n_tr, int* __
 cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const float* lse,
                               const float* sink, float* nlse2, float* delta, float* part, int B,
                               int Hq, int Sq, int Sq_pad, const int* seqlen_q, const int* cu_q,
-                              int total_q, bool overlap_prev, cudaStream_t st) {
+                              int total_q, DevStatus* status, bool overlap_prev, cudaStream_t st) {
   const int nparts = B * (Sq_pad / PREP_BLOCK_ROWS);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(Sq_pad / PREP_BLOCK_ROWS, B * Hq);
@@ -229,9 +234,9 @@ cudaError_t launch_preprocess(bool bf16, const void* O, const void* dO, const fl
   const uint4* o4 = (const uint4*)O;
   const uint4* d4 = (const uint4*)dO;
   return bf16 ? cudaLaunchKernelEx(&cfg, k_preprocess<true>, o4, d4, lse, sink, nlse2, delta, part,
-                                   Hq, Sq, Sq_pad, nparts, seqlen_q, cu_q, total_q)
+                                   Hq, Sq, Sq_pad, nparts, seqlen_q, cu_q, total_q, status)
               : cudaLaunchKernelEx(&cfg, k_preprocess<false>, o4, d4, lse, sink, nlse2, delta,
-                                   part, Hq, Sq, Sq_pad, nparts, seqlen_q, cu_q, total_q);
+                                   part, Hq, Sq, Sq_pad, nparts, seqlen_q, cu_q, total_q, status);
 }
 
 cudaError_t launch_dsink_finalize(const float* part, int Hq, int nparts, float* dsink,
